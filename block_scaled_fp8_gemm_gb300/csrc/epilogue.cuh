@@ -1,0 +1,105 @@
+// epilogue.cuh -- tile bookkeeping and the coalesced row-chunk store shared by
+// the two GEMM kernels.
+#pragma once
+
+#include "kernels.h"
+
+namespace gemmar {
+
+struct TileCoord {
+    int b, p, m0, n0, valid_rows;
+};
+
+template <int BN>
+__device__ __forceinline__ TileCoord decode_tile(int t, const TileGrid &g)
+{
+    TileCoord c;
+    const int nt = t % g.ntiles_n;
+    int r = t / g.ntiles_n;
+    const int mt = r % g.mt_per_band;
+    r /= g.mt_per_band;
+    c.p = r % g.P;
+    c.b = r / g.P;
+    c.m0 = c.b * g.rows_per_band + mt * 128;
+    c.n0 = nt * BN;
+    int band_end = (c.b + 1) * g.rows_per_band;
+    if (band_end > g.M) band_end = g.M;
+    c.valid_rows = min(128, band_end - c.m0);
+    return c;
+}
+
+// Global address of tile row 0 (the caller adds rows) for a tile's output.
+// OUT_PARTIAL_F32 writes W[b][p][row - b*rows_per_band][n].
+__device__ __forceinline__ char *tile_out_base(const GemmOut &o, const TileGrid &g, const TileCoord &c,
+                                               int elem_bytes)
+{
+    int64_t row;
+    if (o.out_mode == OUT_PARTIAL_F32)
+        row = ((int64_t)c.b * g.P + c.p) * g.rows_per_band + (c.m0 - (int64_t)c.b * g.rows_per_band);
+    else
+        row = c.m0;
+    return reinterpret_cast<char *>(o.out) + (row * g.N + c.n0) * elem_bytes;
+}
+
+// Store one 32-row chunk of a warp's output through a warp-private 32 x
+// (UNITS*16)-byte shared staging buffer: each thread writes its own row
+// (16-byte units, XOR-swizzled so the 8 threads of a shared-memory phase hit
+// distinct banks), then the warp reads it back row-contiguously and issues
+// coalesced 16-byte global stores (UNITS lanes per row).  rows_valid masks
+// rows past the band or matrix end.  Whole warp must call.
+template <int UNITS>
+__device__ __forceinline__ void store_chunk(uint32_t stage, const uint4 (&v)[UNITS], char *gdst,
+                                            int64_t row_stride_bytes, int rows_valid)
+{
+    static_assert(UNITS == 8 || UNITS == 4, "chunk is 128 or 64 bytes per row");
+    constexpr int ROWB = UNITS * 16;
+    const int lane = threadIdx.x & 31;
+    const int sw = (UNITS == 8) ? (lane & 7) : ((lane >> 1) & 3);
+#pragma unroll
+    for (int u = 0; u < UNITS; ++u)
+        ptx::st_shared_v4(stage + lane * ROWB + ((u ^ sw) * 16), v[u]);
+    __syncwarp();
+    constexpr int RPI = 32 / UNITS;   // rows per store instruction
+#pragma unroll
+    for (int i = 0; i < UNITS; ++i) {
+        const int r = i * RPI + lane / UNITS;
+        const int u = lane % UNITS;
+        const int rsw = (UNITS == 8) ? (r & 7) : ((r >> 1) & 3);
+        const uint4 val = ptx::ld_shared_v4(stage + r * ROWB + ((u ^ rsw) * 16));
+        if (r < rows_valid)
+            *reinterpret_cast<uint4 *>(gdst + r * row_stride_bytes + u * 16) = val;
+    }
+    __syncwarp();
+}
+
+// Publish one retired tile (per warp) to the band reducer: every lane's
+// stores are made visible at gpu scope, then lane 0 adds 1 with release.
+__device__ __forceinline__ void signal_band(const GemmOut &o, int band)
+{
+    __threadfence();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0 && band != o.skip_band)
+        ptx::red_release_add(o.band_done + band, 1u);
+}
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Round a dynamic shared-memory pointer up to a 1024-byte boundary of the
+// shared address space (the 128-byte swizzle pattern repeats every 1024 bytes).
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p)
+{
+    const uint32_t a = ptx::smem_u32(p);
+    return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+}  // namespace gemmar

@@ -1,0 +1,321 @@
+// gemm_blockscale.cu -- block-scaled e4m3 GEMM on the 5th-generation tensor
+// cores (tcgen05) with the fp32 1x128 (A) and 128x128 (B) scales applied at
+// K-block granularity while draining TMEM ("MORI GEMM + All-Reduce
+// Benchmark", "Running the benchmark": A 1x128, B 128x128, fp32 scales).
+//
+// One persistent CTA per SM, 12 warps, warp-specialised:
+//   warp 0      TMA producer: A tile 128x128 and B tile BNx128 (e4m3, 128-byte
+//               swizzle) per 128-K stage into a STAGES-deep shared ring.
+//   warp 1      MMA issuer: per stage, 4 x tcgen05.mma kind::f8f6f4
+//               (128 x BN x 32) into one of two TMEM accumulators, a fresh
+//               accumulation per K-block (the scale changes every K-block).
+//   warps 4-11  epilogue / scale promotion: each thread owns one tile row and
+//               BN/2 columns in registers and, per K-block, applies
+//               acc += (sa[m,kb] * sb[n/128,kb]) * P_kb as it drains TMEM,
+//               releasing the TMEM buffer back to the MMA warp as soon as it
+//               is read.  At tile end: bf16/fp32 store through shared staging,
+//               or the band-ordered fp32 partial plus a band counter signal.
+// TMEM holds 2 x BN fp32 columns (double-buffered K-blocks), so the tensor
+// cores run K-block kb+1 while the epilogue promotes kb.
+#include "epilogue.cuh"
+
+namespace gemmar {
+using namespace ptx;
+
+namespace {
+
+template <int BN>
+struct BsCfg {
+    static constexpr int kStages = (BN == 256) ? 4 : 6;
+    static constexpr int kABytes = 128 * 128;
+    static constexpr int kBBytes = BN * 128;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kEpiWarps = 8;
+    static constexpr int kStagingBytes = kEpiWarps * 4096;
+    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kStages * kABytes;
+    static constexpr int kOffStaging = kOffB + kStages * kBBytes;
+    static constexpr int kOffBar = kOffStaging + kStagingBytes;
+    static constexpr int kNumBars = 2 * kStages + 5;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kTmemCols <= 512, "TMEM budget");
+};
+
+constexpr int kThreads = 384;
+constexpr int kRegsLow = 56;    // warpgroup 0 (producer, MMA) after setmaxnreg.dec
+constexpr int kRegsHigh = 224;  // warpgroups 1-2 (epilogue) after setmaxnreg.inc
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __grid_constant__ BsParams prm)
+{
+    using C = BsCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *tfull = empty + C::kStages;   // [2]
+    uint64_t *tempty = tfull + 2;           // [2]
+    uint64_t *final_bar = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const TileGrid &g = prm.g;
+    const int KB = g.K / 128;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull + b, 1);
+            mbar_init(tempty + b, C::kEpiWarps);
+        }
+        mbar_init(final_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int p = 0; p < g.P; ++p) {
+            prefetch_tmap(&prm.tmA[p]);
+            prefetch_tmap(&prm.tmB[p]);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp < 4) {
+        setmaxnreg_dec<kRegsLow>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0, issued = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
+                const TileCoord tc = decode_tile<BN>(t, g);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(empty + stage, ph ^ 1, abort_flag, prm.status, prm.timeout_ns,
+                                   SITE_PRODUCER_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full + stage, C::kStageBytes);
+                    tma_load_2d(smem + C::kOffA + stage * C::kABytes, &prm.tmA[tc.p], full + stage, kb * 128, tc.m0);
+                    tma_load_2d(smem + C::kOffB + stage * C::kBBytes, &prm.tmB[tc.p], full + stage, kb * 128, tc.n0);
+                    ++issued;
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (*abort_flag) {
+                // the CTA is giving up: let the loads already in flight land before it exits
+                const int first = issued > C::kStages ? issued - C::kStages : 0;
+                for (int j = first; j < issued; ++j) {
+                    uint64_t *bar = full + (j % C::kStages);
+                    const uint32_t par = (uint32_t)((j / C::kStages) & 1);
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(bar, par) && globaltimer() - t0 < prm.timeout_ns) {
+                    }
+                }
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            const uint32_t idesc = idesc_f8_e4m3(128, BN);
+            int stage = 0;
+            uint32_t ph = 0, kiter = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    const uint32_t buf = kiter & 1, tph = (kiter >> 1) & 1;
+                    if (!mbar_wait(tempty + buf, tph ^ 1, abort_flag, prm.status, prm.timeout_ns,
+                                   SITE_MMA_TMEM_EMPTY) ||
+                        !mbar_wait(full + stage, ph, abort_flag, prm.status, prm.timeout_ns, SITE_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = desc_kmajor_sw128(smem_u32(smem + C::kOffA + stage * C::kABytes));
+                    const uint64_t bd = desc_kmajor_sw128(smem_u32(smem + C::kOffB + stage * C::kBBytes));
+                    const uint32_t d = tmem_base + buf * BN;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)   // 4 x 32 of K = one 128-byte swizzle row
+                        mma_f8(d, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
+                    tc_commit(empty + stage);   // stage reusable once these MMAs have read it
+                    tc_commit(tfull + buf);     // K-block partial ready for promotion
+                    ++kiter;
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            // all MMAs issued by this thread complete before TMEM is released
+            tc_commit(final_bar);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(final_bar, 0)) {
+                if (globaltimer() - t0 > prm.timeout_ns) {
+                    report(prm.status, kErrTimeout, SITE_TEARDOWN_MMA);
+                    break;
+                }
+            }
+        }
+    } else {
+        setmaxnreg_inc<kRegsHigh>();
+        // ---------------------------------------------------- epilogue
+        constexpr int HALF = BN / 2;
+        constexpr int NCH = HALF / 32;   // 32-column chunks per thread (even)
+        static_assert(NCH % 2 == 0, "chunk pipeline works in pairs");
+        const int ew = warp - 4;        // 0..7
+        const int q = warp & 3;         // TMEM lane quarter this warp may access
+        const int h = ew >> 2;          // column half of the tile
+        const int row = q * 32 + lane;  // tile row owned by this thread
+        const uint32_t staging = smem_u32(smem + C::kOffStaging + ew * 4096);
+        const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + h * HALF;
+        uint32_t kiter = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
+            const TileCoord tc = decode_tile<BN>(t, g);
+            const int mrow = min(tc.m0 + row, g.M - 1);
+            const float *sa_row = prm.sa[tc.p] + (int64_t)mrow * KB;
+            const float *sb_blk = prm.sb[tc.p] + (int64_t)((tc.n0 + h * HALF) >> 7) * KB;
+            float acc[HALF];
+#pragma unroll
+            for (int j = 0; j < HALF; ++j)
+                acc[j] = 0.0f;
+            float s_next = __ldg(sa_row) * __ldg(sb_blk);
+            for (int kb = 0; kb < KB; ++kb) {
+                const float s = s_next;
+                if (kb + 1 < KB)
+                    s_next = __ldg(sa_row + kb + 1) * __ldg(sb_blk + kb + 1);
+                const uint32_t buf = kiter & 1, tph = (kiter >> 1) & 1;
+                if (!mbar_wait(tfull + buf, tph, abort_flag, prm.status, prm.timeout_ns, SITE_EPI_TMEM_FULL)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = lane_base + buf * BN;
+                uint32_t ra[32], rb[32];
+                tmem_ld_x32(taddr, ra);
+                tmem_wait_ld(ra);
+#pragma unroll
+                for (int c = 0; c < NCH; c += 2) {
+                    tmem_ld_x32(taddr + (c + 1) * 32, rb);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        acc[c * 32 + j] = fmaf(s, __uint_as_float(ra[j]), acc[c * 32 + j]);
+                    tmem_wait_ld(rb);
+                    if (c + 2 >= NCH) {
+                        // whole K-block read: hand the buffer back to the MMA warp
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(tempty + buf);
+                    } else {
+                        tmem_ld_x32(taddr + (c + 2) * 32, ra);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        acc[(c + 1) * 32 + j] = fmaf(s, __uint_as_float(rb[j]), acc[(c + 1) * 32 + j]);
+                    if (c + 2 < NCH)
+                        tmem_wait_ld(ra);
+                }
+                ++kiter;
+            }
+            if (!ok)
+                break;
+            // -------- tile store
+            const int rows_valid = max(0, min(32, tc.valid_rows - q * 32));
+            if (prm.o.out_mode == OUT_BF16) {
+                char *base = tile_out_base(prm.o, g, tc, 2) + ((int64_t)q * 32 * g.N + h * HALF) * 2;
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    uint4 v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float *a = &acc[c * 32 + u * 8];
+                        v[u] = make_uint4(bf16x2_from_f32(a[0], a[1]), bf16x2_from_f32(a[2], a[3]),
+                                          bf16x2_from_f32(a[4], a[5]), bf16x2_from_f32(a[6], a[7]));
+                    }
+                    store_chunk<4>(staging, v, base + c * 64, (int64_t)g.N * 2, rows_valid);
+                }
+            } else {
+                char *base = tile_out_base(prm.o, g, tc, 4) + ((int64_t)q * 32 * g.N + h * HALF) * 4;
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                    uint4 v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const float *a = &acc[c * 32 + u * 4];
+                        v[u] = make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                                          __float_as_uint(a[3]));
+                    }
+                    store_chunk<8>(staging, v, base + c * 128, (int64_t)g.N * 4, rows_valid);
+                }
+                if (prm.o.out_mode == OUT_PARTIAL_F32)
+                    signal_band(prm.o, tc.b);
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+template <int BN>
+cudaError_t launch_bn(const BsParams &p, int grid, cudaStream_t s)
+{
+    using C = BsCfg<BN>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_blockscale_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+        if (e != cudaSuccess)
+            return e;
+        configured = true;
+    }
+    gemm_blockscale_kernel<BN><<<grid, kThreads, C::kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int BN>
+int regs_of()
+{
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, gemm_blockscale_kernel<BN>) != cudaSuccess)
+        return -1;
+    return a.numRegs;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_blockscale(const BsParams &p, int bn, int grid, cudaStream_t s)
+{
+    if (bn == 256)
+        return launch_bn<256>(p, grid, s);
+    if (bn == 128)
+        return launch_bn<128>(p, grid, s);
+    return cudaErrorInvalidValue;
+}
+
+int gemm_blockscale_num_regs(int bn) { return bn == 256 ? regs_of<256>() : regs_of<128>(); }
+
+int gemm_threads() { return kThreads; }
+
+}  // namespace gemmar

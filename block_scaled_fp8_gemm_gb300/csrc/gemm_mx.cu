@@ -1,0 +1,288 @@
+// gemm_mx.cu -- mxfp8 GEMM (e4m3 with one ue8m0 scale per 32 of K for every
+// row of A and of B; sglang pull request #43480, "What") on the native
+// block-scaled tensor-core MMA: tcgen05.mma kind::mxf8f6f4.block_scale with
+// scale_vec::1X, the scales read from TMEM, accumulation over the whole K in
+// TMEM -- no promotion on the CUDA cores.
+//
+// Same persistent, warp-specialised layout as the blockscale kernel:
+//   warp 0     TMA producer: A 128x128, B BNx128 tiles (128-byte swizzle) and
+//              the stage's repacked scale images (512 + 1024 bytes, bulk copy).
+//   warp 1     MMA issuer: per stage, tcgen05.cp of the scale images into
+//              TMEM (32x128b, replicated to the four lane quarters), then
+//              4 block-scaled MMAs (K = 32 each; scale-factor id k selects the
+//              byte of the 32-bit scale word).  tcgen05.cp and tcgen05.mma
+//              issued by one thread execute in order, so one TMEM scale slot
+//              serves every stage.
+//   warps 4-11 epilogue: drain the tile's fp32 accumulator (double-buffered
+//              across tiles) in 32-column chunks and store it.
+// TMEM: accumulators at columns [0, 2*BN), A scales at 480..483, B scales at
+// 488..495.
+#include "epilogue.cuh"
+
+namespace gemmar {
+using namespace ptx;
+
+namespace {
+
+constexpr uint32_t kSfaCol = 480;
+constexpr uint32_t kSfbCol = 488;
+
+template <int BN>
+struct MxCfg {
+    static constexpr int kStages = (BN == 224) ? 4 : 5;
+    static constexpr int kABytes = 128 * 128;
+    static constexpr int kBBytes = BN * 128;
+    static constexpr int kSfBytes = 512 + 1024;
+    static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
+    static constexpr int kEpiWarps = 8;
+    static constexpr int kStagingBytes = kEpiWarps * 4096;
+    static constexpr int kTmemCols = 512;
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kStages * kABytes;
+    static constexpr int kOffSf = kOffB + kStages * kBBytes;
+    static constexpr int kOffStaging = kOffSf + kStages * kSfBytes;
+    static constexpr int kOffBar = kOffStaging + kStagingBytes;
+    static constexpr int kNumBars = 2 * kStages + 5;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+    static_assert(kBBytes % 1024 == 0, "B tiles stay 1024-byte aligned");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(2 * BN <= (int)kSfaCol, "accumulators below the scale columns");
+};
+
+constexpr int kThreads = 384;
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_constant__ MxParams prm)
+{
+    using C = MxCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *tfull = empty + C::kStages;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *final_bar = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const TileGrid &g = prm.g;
+    const int KB = g.K / 128;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull + b, 1);
+            mbar_init(tempty + b, C::kEpiWarps);
+        }
+        mbar_init(final_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int p = 0; p < g.P; ++p) {
+            prefetch_tmap(&prm.tmA[p]);
+            prefetch_tmap(&prm.tmB[p]);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0, issued = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
+                const TileCoord tc = decode_tile<BN>(t, g);
+                const int mt = (tc.m0 - tc.b * g.rows_per_band) / 128;
+                const int64_t a_img = ((int64_t)(tc.p * g.bands + tc.b) * g.mt_per_band + mt) * KB;
+                const int64_t b_img = ((int64_t)tc.p * g.ntiles_n + tc.n0 / BN) * KB;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(empty + stage, ph ^ 1, abort_flag, prm.status, prm.timeout_ns,
+                                   SITE_PRODUCER_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sf = smem + C::kOffSf + stage * C::kSfBytes;
+                    mbar_arrive_expect_tx(full + stage, C::kStageBytes);
+                    tma_load_2d(smem + C::kOffA + stage * C::kABytes, &prm.tmA[tc.p], full + stage, kb * 128, tc.m0);
+                    tma_load_2d(smem + C::kOffB + stage * C::kBBytes, &prm.tmB[tc.p], full + stage, kb * 128, tc.n0);
+                    bulk_load(sf, prm.sfa + (a_img + kb) * 512, 512, full + stage);
+                    bulk_load(sf + 512, prm.sfb + (b_img + kb) * 1024, 1024, full + stage);
+                    ++issued;
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (*abort_flag) {
+                const int first = issued > C::kStages ? issued - C::kStages : 0;
+                for (int j = first; j < issued; ++j) {
+                    uint64_t *bar = full + (j % C::kStages);
+                    const uint32_t par = (uint32_t)((j / C::kStages) & 1);
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(bar, par) && globaltimer() - t0 < prm.timeout_ns) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            int stage = 0;
+            uint32_t ph = 0, titer = 0;
+            bool ok = true;
+            const uint32_t sfa_t = tmem_base + kSfaCol, sfb_t = tmem_base + kSfbCol;
+            for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
+                const uint32_t buf = titer & 1, tph = (titer >> 1) & 1;
+                if (!mbar_wait(tempty + buf, tph ^ 1, abort_flag, prm.status, prm.timeout_ns,
+                               SITE_MMA_TMEM_EMPTY))
+                    break;
+                const uint32_t d = tmem_base + buf * BN;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(full + stage, ph, abort_flag, prm.status, prm.timeout_ns, SITE_MMA_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sf = smem_u32(smem + C::kOffSf + stage * C::kSfBytes);
+                    tc_cp_32x128b_warpx4(sfa_t, smem_desc(sf, 0, 128, 0));
+                    tc_cp_32x128b_warpx4(sfb_t, smem_desc(sf + 512, 0, 128, 0));
+                    tc_cp_32x128b_warpx4(sfb_t + 4, smem_desc(sf + 768, 0, 128, 0));
+                    const uint64_t ad = desc_kmajor_sw128(smem_u32(smem + C::kOffA + stage * C::kABytes));
+                    const uint64_t bd = desc_kmajor_sw128(smem_u32(smem + C::kOffB + stage * C::kBBytes));
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        mma_mxf8(d, ad + 2 * k, bd + 2 * k, idesc_mx_e4m3(128, BN, (uint32_t)k), sfa_t, sfb_t,
+                                 (kb > 0 || k > 0) ? 1u : 0u);
+                    tc_commit(empty + stage);
+                    if (kb == KB - 1)
+                        tc_commit(tfull + buf);
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        ph ^= 1;
+                    }
+                }
+                ++titer;
+            }
+            tc_commit(final_bar);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(final_bar, 0)) {
+                if (globaltimer() - t0 > prm.timeout_ns) {
+                    report(prm.status, kErrTimeout, SITE_TEARDOWN_MMA);
+                    break;
+                }
+            }
+        }
+    } else if (warp >= 4) {
+        // ---------------------------------------------------- epilogue
+        constexpr int NCH = BN / 32;
+        const int ew = warp - 4;
+        const int q = warp & 3;
+        const int h = ew >> 2;
+        const uint32_t staging = smem_u32(smem + C::kOffStaging + ew * 4096);
+        const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+        uint32_t titer = 0;
+        for (int t = blockIdx.x; t < g.num_tiles; t += gridDim.x) {
+            const TileCoord tc = decode_tile<BN>(t, g);
+            const uint32_t buf = titer & 1, tph = (titer >> 1) & 1;
+            if (!mbar_wait(tfull + buf, tph, abort_flag, prm.status, prm.timeout_ns, SITE_EPI_TMEM_FULL))
+                break;
+            tc_fence_after();
+            const int rows_valid = max(0, min(32, tc.valid_rows - q * 32));
+            const int esz = prm.o.out_mode == OUT_BF16 ? 2 : 4;
+            char *base = tile_out_base(prm.o, g, tc, esz) + (int64_t)q * 32 * g.N * esz;
+            for (int c = h; c < NCH; c += 2) {
+                uint32_t r[32];
+                tmem_ld_x32(lane_base + buf * BN + c * 32, r);
+                tmem_wait_ld(r);
+                if (c + 2 >= NCH) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(tempty + buf);
+                }
+                if (prm.o.out_mode == OUT_BF16) {
+                    uint4 v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        v[u] = make_uint4(bf16x2_from_f32(__uint_as_float(r[u * 8 + 0]), __uint_as_float(r[u * 8 + 1])),
+                                          bf16x2_from_f32(__uint_as_float(r[u * 8 + 2]), __uint_as_float(r[u * 8 + 3])),
+                                          bf16x2_from_f32(__uint_as_float(r[u * 8 + 4]), __uint_as_float(r[u * 8 + 5])),
+                                          bf16x2_from_f32(__uint_as_float(r[u * 8 + 6]), __uint_as_float(r[u * 8 + 7])));
+                    store_chunk<4>(staging, v, base + c * 64, (int64_t)g.N * 2, rows_valid);
+                } else {
+                    uint4 v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        v[u] = make_uint4(r[u * 4 + 0], r[u * 4 + 1], r[u * 4 + 2], r[u * 4 + 3]);
+                    store_chunk<8>(staging, v, base + c * 128, (int64_t)g.N * 4, rows_valid);
+                }
+            }
+            if (prm.o.out_mode == OUT_PARTIAL_F32)
+                signal_band(prm.o, tc.b);
+            ++titer;
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        tmem_dealloc(tmem_base, C::kTmemCols);
+}
+
+template <int BN>
+cudaError_t launch_bn(const MxParams &p, int grid, cudaStream_t s)
+{
+    using C = MxCfg<BN>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e =
+            cudaFuncSetAttribute(gemm_mx_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess)
+            return e;
+        configured = true;
+    }
+    gemm_mx_kernel<BN><<<grid, kThreads, C::kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int BN>
+int regs_of()
+{
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, gemm_mx_kernel<BN>) != cudaSuccess)
+        return -1;
+    return a.numRegs;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_mx(const MxParams &p, int bn, int grid, cudaStream_t s)
+{
+    if (bn == 224)
+        return launch_bn<224>(p, grid, s);
+    if (bn == 128)
+        return launch_bn<128>(p, grid, s);
+    return cudaErrorInvalidValue;
+}
+
+int gemm_mx_num_regs(int bn) { return bn == 224 ? regs_of<224>() : regs_of<128>(); }
+
+}  // namespace gemmar

@@ -1,0 +1,86 @@
+// kernels.h -- host-side launch interface between the C ABI (gemmar.cu) and
+// the kernel translation units.  Internal to libgemmar.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace gemmar {
+
+constexpr int kMaxP = 8;      // == GEMMAR_MAX_P
+constexpr int kMaxBands = 1024;
+
+enum OutMode : int {
+    OUT_PARTIAL_F32 = 0,   // fp32 partial into W[band][p][row-in-band][N], then signal the band counter
+    OUT_F32 = 1,           // fp32 C[M,N]
+    OUT_BF16 = 2,          // bf16 C[M,N]
+};
+
+// Work decomposition shared by both GEMM kernels: tile t covers rows
+// [m0, m0 + min(128, band end - m0)) and columns [n0, n0 + BN) of slice p in
+// band b, with t = ((b * P + p) * mt_per_band + mt) * ntiles_n + nt, i.e. in
+// band order so that band 0's partials are complete first.
+struct TileGrid {
+    int P, M, N, K;
+    int bands, rows_per_band, mt_per_band, ntiles_n, num_tiles;
+};
+
+struct GemmOut {
+    void *out;               // W (OUT_PARTIAL_F32) or C
+    uint32_t *band_done;     // per-band tile-retire counters (OUT_PARTIAL_F32)
+    int out_mode;
+    int skip_band;           // fault injection: this band is never signalled (-1: none)
+};
+
+struct BsParams {
+    CUtensorMap tmA[kMaxP];  // A_p: dims {K, M} bytes, box {128, 128}, 128B swizzle
+    CUtensorMap tmB[kMaxP];  // B_p: dims {K, N} bytes, box {128, BN}, 128B swizzle
+    const float *sa[kMaxP];  // [M, K/128]
+    const float *sb[kMaxP];  // [N/128, K/128]
+    TileGrid g;
+    GemmOut o;
+    ptx::DevStatus *status;
+    uint64_t timeout_ns;
+};
+
+struct MxParams {
+    CUtensorMap tmA[kMaxP];
+    CUtensorMap tmB[kMaxP];
+    const uint8_t *sfa;      // repacked A scale words: [P][bands][mt_per_band][K/128][512 B]
+    const uint8_t *sfb;      // repacked B scale words: [P][N/BN][K/128][1024 B]
+    TileGrid g;
+    GemmOut o;
+    ptx::DevStatus *status;
+    uint64_t timeout_ns;
+};
+
+// GEMM launchers (bn: 256 or 128 for blockscale; 224 or 128 for mx).
+cudaError_t launch_gemm_blockscale(const BsParams &p, int bn, int grid, cudaStream_t s);
+cudaError_t launch_gemm_mx(const MxParams &p, int bn, int grid, cudaStream_t s);
+// Register count each GEMM kernel was built with (the warp-role register split needs it).
+int gemm_blockscale_num_regs(int bn);
+int gemm_mx_num_regs(int bn);
+int gemm_threads();
+
+// Scale repack for the mx GEMM (row-major ue8m0 bytes -> the tcgen05.cp image).
+// ea/eb are host arrays of P device pointers.  Image layout: see streaming.cu.
+cudaError_t launch_mx_repack(const uint8_t *const *ea, const uint8_t *const *eb, int P, int M, int N, int K,
+                             int bands, int bn, uint8_t *sfa_out, uint8_t *sfb_out, cudaStream_t s);
+
+// Streaming kernels.
+cudaError_t launch_band_reduce(const float *W, uint16_t *out, int P, int64_t M, int64_t N, int bands,
+                               const uint32_t *band_done, uint32_t expected, ptx::DevStatus *status,
+                               uint64_t timeout_ns, int grid_blocks, cudaStream_t s);
+cudaError_t launch_rowquant(const void *x, int x_is_bf16, int64_t M, int64_t N, uint8_t *q, float *s,
+                            int num_sms, cudaStream_t st);
+cudaError_t launch_rowdequant(const uint8_t *q, const float *s, int64_t M, int64_t N, uint16_t *y, int num_sms,
+                              cudaStream_t st);
+cudaError_t launch_quant_blockscale(const float *x, int64_t R, int64_t C, int group_rows, uint8_t *q,
+                                    float *scales, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_mx(const float *x, int64_t R, int64_t C, uint8_t *q, uint8_t *e8, int num_sms,
+                            cudaStream_t st);
+
+}  // namespace gemmar

@@ -1,0 +1,441 @@
+// streaming.cu -- the HBM-bound kernels of the path: the fixed-order band
+// reduce, the per-row e4m3 codec (fp8 wire), the device quantisers and the
+// mxfp8 scale repack.  All are coalesced, 16-byte vectorised, grid-stride
+// kernels sized in multiples of the SM count.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+
+namespace gemmar {
+using namespace ptx;
+
+namespace {
+
+__host__ __device__ inline int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ inline int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+__device__ __forceinline__ float4 ldcg4(const float *p) { return __ldcg(reinterpret_cast<const float4 *>(p)); }
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// --------------------------------------------------------------------------
+// band_reduce: out[m,n] = bf16_rn(((W[b][0] + W[b][1]) + ...) + W[b][P-1]), fp32,
+// p ascending.  One thread reduces 8 consecutive columns of one row across all
+// P slices with 2P independent 16-byte loads in flight.  When band_done is
+// given, the CTA first waits (bounded) until that band's tiles have all
+// retired; the counter is read with acquire semantics and W with L2-coherent
+// (.cg) loads.
+// --------------------------------------------------------------------------
+template <int P>
+__global__ void __launch_bounds__(256) band_reduce_kernel(const float *__restrict__ W, uint16_t *__restrict__ out,
+                                                          int64_t rows_per_band, int64_t N, int bands,
+                                                          const uint32_t *band_done, uint32_t expected,
+                                                          DevStatus *status, uint64_t timeout_ns)
+{
+    __shared__ int band_ok;
+    const int64_t band_elems = rows_per_band * N;
+    const int64_t npk = band_elems / 8;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int b = 0; b < bands; ++b) {
+        if (band_done != nullptr) {
+            if (threadIdx.x == 0) {
+                int ok = 1;
+                if (ld_acquire(band_done + b) < expected) {
+                    const uint64_t t0 = globaltimer();
+                    while (ld_acquire(band_done + b) < expected) {
+                        if (*(volatile int *)&status->code != 0) { ok = 0; break; }
+                        if (globaltimer() - t0 > timeout_ns) {
+                            report(status, kErrTimeout, SITE_REDUCE_BAND);
+                            ok = 0;
+                            break;
+                        }
+                        __nanosleep(256);
+                    }
+                }
+                band_ok = ok;
+            }
+            __syncthreads();
+            if (!band_ok)
+                return;
+        }
+        const float *Wb = W + (int64_t)b * P * band_elems;
+        uint16_t *ob = out + (int64_t)b * band_elems;
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < npk; i += stride) {
+            const float *src = Wb + i * 8;
+            float4 lo[P], hi[P];
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                lo[p] = ldcg4(src + p * band_elems);
+                hi[p] = ldcg4(src + p * band_elems + 4);
+            }
+            float4 a = lo[0], c = hi[0];
+#pragma unroll
+            for (int p = 1; p < P; ++p) {
+                a.x = a.x + lo[p].x; a.y = a.y + lo[p].y; a.z = a.z + lo[p].z; a.w = a.w + lo[p].w;
+                c.x = c.x + hi[p].x; c.y = c.y + hi[p].y; c.z = c.z + hi[p].z; c.w = c.w + hi[p].w;
+            }
+            uint4 o;
+            o.x = bf16x2_from_f32(a.x, a.y);
+            o.y = bf16x2_from_f32(a.z, a.w);
+            o.z = bf16x2_from_f32(c.x, c.y);
+            o.w = bf16x2_from_f32(c.z, c.w);
+            *reinterpret_cast<uint4 *>(ob + i * 8) = o;
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// rowquant: one warp per row.  Pass 1 streams the row for its amax (warp
+// shuffle max); pass 2 re-reads it (L1/L2 hit) and writes the codes.
+// s = fp32(amax / 448) and codes = e4m3_rn_sat(fp32(x / s)), IEEE divisions.
+// --------------------------------------------------------------------------
+template <bool BF16>
+__device__ __forceinline__ void load8(const void *x, int64_t idx, float (&v)[8])
+{
+    if constexpr (BF16) {
+        uint4 w = *reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(x) + idx);
+        v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+        v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+    } else {
+        const float *f = reinterpret_cast<const float *>(x) + idx;
+        float4 a = *reinterpret_cast<const float4 *>(f);
+        float4 b = *reinterpret_cast<const float4 *>(f + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+}
+
+__device__ __forceinline__ uint32_t enc4(float a, float b, float c, float d, float s)
+{
+    if (s == 0.0f)
+        return 0u;
+    uint32_t lo = e4m3x2_from_f32(__fdiv_rn(a, s), __fdiv_rn(b, s));
+    uint32_t hi = e4m3x2_from_f32(__fdiv_rn(c, s), __fdiv_rn(d, s));
+    return lo | (hi << 16);
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) rowquant_kernel(const void *__restrict__ x, int64_t M, int64_t N,
+                                                       uint8_t *__restrict__ q, float *__restrict__ s)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < M; row += warps_total) {
+        const int64_t base = row * N;
+        float amax = 0.0f;
+#pragma unroll 4
+        for (int64_t c = (int64_t)lane * 8; c < N; c += 256) {
+            float v[8];
+            load8<BF16>(x, base + c, v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                amax = fmaxf(amax, fabsf(v[j]));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float sc = __fdiv_rn(amax, 448.0f);
+        if (lane == 0)
+            s[row] = sc;
+#pragma unroll 4
+        for (int64_t c = (int64_t)lane * 8; c < N; c += 256) {
+            float v[8];
+            load8<BF16>(x, base + c, v);
+            uint2 w;
+            w.x = enc4(v[0], v[1], v[2], v[3], sc);
+            w.y = enc4(v[4], v[5], v[6], v[7], sc);
+            *reinterpret_cast<uint2 *>(q + base + c) = w;
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// rowdequant: y = bf16_rn(fp32(decode(q) * s[row])), 16 codes per thread.
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) rowdequant_kernel(const uint8_t *__restrict__ q, const float *__restrict__ s,
+                                                         int64_t M, int64_t N, uint16_t *__restrict__ y)
+{
+    const int64_t n16 = M * N / 16;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
+        const int64_t e = i * 16;
+        const float sc = __ldg(s + e / N);
+        const uint4 c = __ldcs(reinterpret_cast<const uint4 *>(q + e));
+        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float2 a = f32x2_from_e4m3x2((uint16_t)(w[j] & 0xFFFFu));
+            float2 b = f32x2_from_e4m3x2((uint16_t)(w[j] >> 16));
+            o[2 * j] = bf16x2_from_f32(__fmul_rn(a.x, sc), __fmul_rn(a.y, sc));
+            o[2 * j + 1] = bf16x2_from_f32(__fmul_rn(b.x, sc), __fmul_rn(b.y, sc));
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(y + e);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// --------------------------------------------------------------------------
+// Blockscale quantisers.  1x128: one warp per (row, 128-group), 4 values per
+// lane.  128x128: one 256-thread CTA per block.  s = fp32(amax/448),
+// codes = e4m3_rn_sat(fp32(x/s)); zero group -> s = 0, +0 codes.
+// --------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) quant_1x128_kernel(const float *__restrict__ x, int64_t R, int64_t C,
+                                                          uint8_t *__restrict__ q, float *__restrict__ scales)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t G = C / 128;
+    const int64_t ngroups = R * G;
+    const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t gi = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); gi < ngroups; gi += warps_total) {
+        const int64_t r = gi / G, g = gi % G;
+        const int64_t e = r * C + g * 128 + lane * 4;
+        const float4 v = *reinterpret_cast<const float4 *>(x + e);
+        float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const float sc = __fdiv_rn(amax, 448.0f);
+        if (lane == 0)
+            scales[gi] = sc;
+        *reinterpret_cast<uint32_t *>(q + e) = enc4(v.x, v.y, v.z, v.w, sc);
+    }
+}
+
+__global__ void __launch_bounds__(256) quant_128x128_kernel(const float *__restrict__ x, int64_t R, int64_t C,
+                                                            uint8_t *__restrict__ q, float *__restrict__ scales)
+{
+    __shared__ float red[8];
+    const int64_t G = C / 128;
+    const int64_t nblk = ((R + 127) / 128) * G;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int64_t bi = blockIdx.x; bi < nblk; bi += gridDim.x) {
+        const int64_t br = bi / G, bc = bi % G;
+        const int64_t r0 = br * 128;
+        const int rows = (int)min64(128, R - r0);
+        // thread covers column quad (tid & 31)*4 of rows (tid >> 5) + 8*j
+        float amax = 0.0f;
+        for (int rr = warp; rr < rows; rr += 8) {
+            const float4 v = *reinterpret_cast<const float4 *>(x + (r0 + rr) * C + bc * 128 + lane * 4);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        if (lane == 0)
+            red[warp] = amax;
+        __syncthreads();
+        float m = red[0];
+#pragma unroll
+        for (int w = 1; w < 8; ++w)
+            m = fmaxf(m, red[w]);
+        const float sc = __fdiv_rn(m, 448.0f);
+        if (tid == 0)
+            scales[bi] = sc;
+        for (int rr = warp; rr < rows; rr += 8) {
+            const int64_t e = (r0 + rr) * C + bc * 128 + lane * 4;
+            const float4 v = *reinterpret_cast<const float4 *>(x + e);
+            *reinterpret_cast<uint32_t *>(q + e) = enc4(v.x, v.y, v.z, v.w, sc);
+        }
+        __syncthreads();
+    }
+}
+
+// ue8m0 byte of r = fp32(amax/448): ceil(log2 r) + 127 from the IEEE fields,
+// exact at powers of two; 0 for r == 0; clamped to [0, 254].
+__device__ __forceinline__ uint32_t ue8m0_of(float r)
+{
+    const uint32_t bits = __float_as_uint(r);
+    if (r == 0.0f)
+        return 0u;
+    const uint32_t ef = (bits >> 23) & 0xFFu, man = bits & 0x7FFFFFu;
+    int e;
+    if (ef == 0) {   // subnormal: man * 2^-149
+        const int fl = (31 - __clz(man)) - 149;
+        e = fl + ((__popc(man) == 1) ? 0 : 1);
+    } else {
+        e = (int)ef - 127 + (man != 0 ? 1 : 0);
+    }
+    int b = e + 127;
+    b = b < 0 ? 0 : (b > 254 ? 254 : b);
+    return (uint32_t)b;
+}
+
+// 2^(127 - byte) as fp32 (byte 254 -> 2^-127, a subnormal).
+__device__ __forceinline__ float inv_scale_of(uint32_t byte)
+{
+    return byte == 254u ? __uint_as_float(0x00400000u) : __uint_as_float((254u - byte) << 23);
+}
+
+// mx quantiser: 8 lanes per 32-wide group, 4 values per lane.
+__global__ void __launch_bounds__(256) quant_mx_kernel(const float *__restrict__ x, int64_t R, int64_t C,
+                                                       uint8_t *__restrict__ q, uint8_t *__restrict__ e8)
+{
+    const int64_t nquads = R * C / 4;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    // the grid stride is a multiple of 32 threads, so the 8 lanes of one group stay together
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nquads; i += stride) {
+        const int64_t e = i * 4;
+        const float4 v = *reinterpret_cast<const float4 *>(x + e);
+        float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+        const uint32_t gmask = 0xFFu << (threadIdx.x & 24);
+        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 4));
+        const uint32_t b = ue8m0_of(__fdiv_rn(amax, 448.0f));
+        if ((threadIdx.x & 7) == 0)
+            e8[e / 32] = (uint8_t)b;
+        uint32_t w = 0;
+        if (amax != 0.0f) {
+            const float inv = inv_scale_of(b);
+            w = e4m3x2_from_f32(__fmul_rn(v.x, inv), __fmul_rn(v.y, inv)) |
+                (e4m3x2_from_f32(__fmul_rn(v.z, inv), __fmul_rn(v.w, inv)) << 16);
+        }
+        *reinterpret_cast<uint32_t *>(q + e) = w;
+    }
+}
+
+// --------------------------------------------------------------------------
+// mx scale repack.  The block-scaled MMA reads the scale of row r (of A, or
+// of B along N) for 32-wide K group j of a 128-K stage from TMEM column
+// base + r/32, lane r%32, byte j.  tcgen05.cp 32x128b copies shared-memory
+// row l (16 bytes = 4 words) into lane l, columns +0..+3, so the image of
+// one stage is word[l*4 + c] = scale word of row c*32 + l (rows past the
+// tile: 0).  A: one 512-byte image per (slice, band, 128-row tile of the
+// band, stage), following the GEMM's tile decomposition; B: two per (slice,
+// BN-column tile, stage) -> rows 0..127 and 128..255 of the tile.
+// --------------------------------------------------------------------------
+struct SlicePtrs {
+    const uint8_t *p[kMaxP];
+};
+
+__global__ void mx_repack_a_kernel(SlicePtrs ea, int P, int M, int K, int bands, int rows_per_band,
+                                   int mt_per_band, uint32_t *__restrict__ out)
+{
+    const int KB = K / 128, G = K / 32;
+    const int64_t total = (int64_t)P * bands * mt_per_band * KB * 128;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int w = (int)(i % 128);
+        int64_t r = i / 128;
+        const int kb = (int)(r % KB); r /= KB;
+        const int mt = (int)(r % mt_per_band); r /= mt_per_band;
+        const int b = (int)(r % bands);
+        const int p = (int)(r / bands);
+        const int lane = w >> 2, c = w & 3;
+        const int band_end = min((b + 1) * rows_per_band, M);
+        const int row = b * rows_per_band + mt * 128 + c * 32 + lane;
+        uint32_t v = 0;
+        if (row < band_end)
+            v = *reinterpret_cast<const uint32_t *>(ea.p[p] + (int64_t)row * G + kb * 4);
+        out[i] = v;
+    }
+}
+
+__global__ void mx_repack_b_kernel(SlicePtrs eb, int P, int N, int K, int BN, uint32_t *__restrict__ out)
+{
+    const int KB = K / 128, NT = N / BN, G = K / 32;
+    const int64_t total = (int64_t)P * NT * KB * 256;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int w = (int)(i % 256);
+        int64_t r = i / 256;
+        const int kb = (int)(r % KB); r /= KB;
+        const int nt = (int)(r % NT);
+        const int p = (int)(r / NT);
+        const int half = w >> 7, lane = (w & 127) >> 2, c = w & 3;
+        const int rt = half * 128 + c * 32 + lane;   // row within the BN tile
+        uint32_t v = 0;
+        if (rt < BN)
+            v = *reinterpret_cast<const uint32_t *>(eb.p[p] + (int64_t)(nt * BN + rt) * G + kb * 4);
+        out[i] = v;
+    }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ launchers
+
+cudaError_t launch_band_reduce(const float *W, uint16_t *out, int P, int64_t M, int64_t N, int bands,
+                               const uint32_t *band_done, uint32_t expected, DevStatus *status,
+                               uint64_t timeout_ns, int grid_blocks, cudaStream_t s)
+{
+    const int64_t rpb = M / bands;
+    dim3 grid(grid_blocks), block(256);
+#define GEMMAR_REDUCE_CASE(PP)                                                                            \
+    case PP:                                                                                              \
+        band_reduce_kernel<PP><<<grid, block, 0, s>>>(W, out, rpb, N, bands, band_done, expected, status, \
+                                                      timeout_ns);                                        \
+        break;
+    switch (P) {
+        GEMMAR_REDUCE_CASE(1) GEMMAR_REDUCE_CASE(2) GEMMAR_REDUCE_CASE(3) GEMMAR_REDUCE_CASE(4)
+        GEMMAR_REDUCE_CASE(5) GEMMAR_REDUCE_CASE(6) GEMMAR_REDUCE_CASE(7) GEMMAR_REDUCE_CASE(8)
+        default: return cudaErrorInvalidValue;
+    }
+#undef GEMMAR_REDUCE_CASE
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rowquant(const void *x, int x_is_bf16, int64_t M, int64_t N, uint8_t *q, float *s, int num_sms,
+                            cudaStream_t st)
+{
+    const int64_t blocks_needed = (M + 7) / 8;
+    const int grid = (int)min64(blocks_needed, (int64_t)num_sms * 8);
+    if (x_is_bf16)
+        rowquant_kernel<true><<<grid, 256, 0, st>>>(x, M, N, q, s);
+    else
+        rowquant_kernel<false><<<grid, 256, 0, st>>>(x, M, N, q, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rowdequant(const uint8_t *q, const float *s, int64_t M, int64_t N, uint16_t *y, int num_sms,
+                              cudaStream_t st)
+{
+    const int64_t need = (M * N / 16 + 255) / 256;
+    const int grid = (int)max64(1, min64(need, (int64_t)num_sms * 8));
+    rowdequant_kernel<<<grid, 256, 0, st>>>(q, s, M, N, y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_blockscale(const float *x, int64_t R, int64_t C, int group_rows, uint8_t *q,
+                                    float *scales, int num_sms, cudaStream_t st)
+{
+    if (group_rows == 1) {
+        const int64_t need = (R * (C / 128) + 7) / 8;
+        const int grid = (int)max64(1, min64(need, (int64_t)num_sms * 8));
+        quant_1x128_kernel<<<grid, 256, 0, st>>>(x, R, C, q, scales);
+    } else {
+        const int64_t nblk = ((R + 127) / 128) * (C / 128);
+        const int grid = (int)max64(1, min64(nblk, (int64_t)num_sms * 8));
+        quant_128x128_kernel<<<grid, 256, 0, st>>>(x, R, C, q, scales);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_mx(const float *x, int64_t R, int64_t C, uint8_t *q, uint8_t *e8, int num_sms,
+                            cudaStream_t st)
+{
+    const int64_t need = (R * C / 4 + 255) / 256;
+    const int grid = (int)max64(1, min64(need, (int64_t)num_sms * 8));
+    quant_mx_kernel<<<grid, 256, 0, st>>>(x, R, C, q, e8);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mx_repack(const uint8_t *const *ea, const uint8_t *const *eb, int P, int M, int N, int K,
+                             int bands, int bn, uint8_t *sfa_out, uint8_t *sfb_out, cudaStream_t s)
+{
+    SlicePtrs pa{}, pb{};
+    for (int p = 0; p < P; ++p) {
+        pa.p[p] = ea[p];
+        pb.p[p] = eb[p];
+    }
+    const int rpb = M / bands, mtpb = (rpb + 127) / 128;
+    const int64_t ta = (int64_t)P * bands * mtpb * (K / 128) * 128;
+    const int64_t tb = (int64_t)P * (N / bn) * (K / 128) * 256;
+    const int ga = (int)max64(1, min64((ta + 255) / 256, 4096));
+    const int gb = (int)max64(1, min64((tb + 255) / 256, 4096));
+    mx_repack_a_kernel<<<ga, 256, 0, s>>>(pa, P, M, K, bands, rpb, mtpb, reinterpret_cast<uint32_t *>(sfa_out));
+    mx_repack_b_kernel<<<gb, 256, 0, s>>>(pb, P, N, K, bn, reinterpret_cast<uint32_t *>(sfb_out));
+    return cudaGetLastError();
+}
+
+}  // namespace gemmar

@@ -1,0 +1,253 @@
+/*
+ * gemmar.h -- C ABI of libgemmar: the block-scaled fp8 GEMM and row-parallel
+ * reduce of a DeepSeek-style attention block's output projection (wo_b),
+ * run on one GB300 GPU (sm_103a).
+ *
+ * What the path computes (sources are web pages, cited by title and section):
+ *   - wo_b is a row-parallel linear layer: a block-scale fp8 GEMM whose
+ *     [M, hidden] result is all-reduced over the ranks that each hold one
+ *     K-slice of the weight (sglang pull request #40757, "What").
+ *   - Quantisation "blockscale": A (activations) with one fp32 scale per 1x128
+ *     group along K, B (weight) with one fp32 scale per 128x128 block
+ *     ("MORI GEMM + All-Reduce Benchmark", "Running the benchmark").
+ *   - Quantisation "mxfp8": e4m3 with a ue8m0 power-of-two scale per 1x32 group,
+ *     the exponent taken from the IEEE bits (sglang pull request #43480,
+ *     "What" and review item 7 "Duplicated ue8m0 scale rule").
+ *   - The reduce accumulates in fp32 and the output is bf16; the optional
+ *     "fp8 wire" sends each output row as e4m3 with one fp32 scale
+ *     ("MORI GEMM + All-Reduce Benchmark", "The fp8 wire").
+ *   - The fused kernel writes each destination's row band as soon as that
+ *     band's tiles are done (sglang pull request #40757, "What"; MORI page,
+ *     "Where the time goes").
+ *
+ * On one GPU the P "ranks" are P K-slices resident in this GPU's memory; the
+ * exchange is the band reduce reading their fp32 partials.  No collective runs.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, row-major,
+ *     contiguous, 16-byte aligned (else GEMMAR_ERR_ALIGN).  Sizes are element
+ *     counts.  e4m3 tensors are uint8 codes (OCP E4M3FN); bf16 tensors are
+ *     uint16 bit patterns.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; 0 = legacy
+ *     default stream) and returns a host status at once.  Any status other
+ *     than GEMMAR_OK returned by a call means nothing was launched, except
+ *     GEMMAR_ERR_CUDA, which reports that a launch or CUDA call failed.
+ *   - Device-side failures (a bounded wait that expired) are recorded in the
+ *     context's device status word; gemmar_status() reads it after the work is
+ *     complete and makes the context sticky-disabled: every later call
+ *     returns GEMMAR_ERR_DISABLED.  No kernel traps, hangs or faults on
+ *     purpose; every device wait has a time limit.
+ *   - The context owns only its workspace (fp32 partials, band counters,
+ *     scale repack area, fp8-wire staging) and status word.  The workspace is
+ *     overwritten by the next call that uses it; calls on one context must be
+ *     stream-ordered (the same stream, or joined by events).
+ *   - The current CUDA device must be the context's device.
+ */
+#ifndef GEMMAR_H
+#define GEMMAR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gemmar_ctx gemmar_ctx;
+
+/* Status codes. */
+enum {
+    GEMMAR_OK = 0,
+    GEMMAR_ERR_ARG = 1,        /* NULL pointer, bad enum value, negative or zero size */
+    GEMMAR_ERR_SHAPE = 2,      /* shape the kernels cannot express (see gemmar_supports) */
+    GEMMAR_ERR_ALIGN = 3,      /* a pointer is not 16-byte aligned */
+    GEMMAR_ERR_WORKSPACE = 4,  /* call needs more workspace than gemmar_create sized */
+    GEMMAR_ERR_CUDA = 5,       /* a CUDA runtime or driver call failed */
+    GEMMAR_ERR_TIMEOUT = 6,    /* a device-side bounded wait expired (read by gemmar_status) */
+    GEMMAR_ERR_DISABLED = 7,   /* context disabled by an earlier device-side failure */
+    GEMMAR_ERR_DEVICE = 8      /* not an sm_103 device, wrong current device, or self-test mismatch */
+};
+
+/* Element types of an output or input matrix. */
+enum { GEMMAR_DTYPE_F32 = 0, GEMMAR_DTYPE_BF16 = 1 };
+
+/* Scale kinds. BLOCK128: fp32 A scales [M, K/128], fp32 B scales [N/128, K/128].
+ * MX32: ue8m0 bytes (value 2^(byte-127)), A [M, K/32], B [N, K/32]. */
+enum { GEMMAR_SCALE_BLOCK128 = 0, GEMMAR_SCALE_MX32 = 1 };
+
+/* Flags of gemmar_create and fused_gemm_reduce. */
+#define GEMMAR_FP8_WIRE        (1u << 0)  /* fused: per-row e4m3 quantise + dequantise of the output */
+#define GEMMAR_DEBUG_CANARY    (1u << 1)  /* fused: pre-fill partials and output with NaN */
+#define GEMMAR_FAULT_SKIP_BAND (1u << 2)  /* fused, testing only: band 0 is never signalled, so the
+                                             reducer's bounded wait expires (GEMMAR_ERR_TIMEOUT) */
+#define GEMMAR_NO_SELF_TEST    (1u << 3)  /* create: skip the closed-form self-test */
+
+/* Largest number of K-slices ("ranks") one call takes. */
+#define GEMMAR_MAX_P 8
+
+/*
+ * gemmar_supports -- can the kernels express this shape?  (The pages' op has
+ * the same question answered by its supports(); sglang pull request #40757,
+ * "Worth a reviewer's attention", last item.)  Rules:
+ *   M >= 1; 1 <= P <= GEMMAR_MAX_P; 1 <= bands <= min(M, 1024) and M % bands == 0;
+ *   BLOCK128: N % 128 == 0 (the B scale block); MX32: N % 128 == 0 or N % 224 == 0;
+ *   K % 128 == 0 (both scale kinds: one MMA stage is 128 of K);
+ *   N <= 65536, K <= 65536, M <= 2^24.
+ * Returns GEMMAR_OK or GEMMAR_ERR_SHAPE / GEMMAR_ERR_ARG.  Needs no GPU.
+ */
+int gemmar_supports(int P, int64_t M, int64_t N, int64_t K, int bands, int scale_kind);
+
+/*
+ * gemmar_create -- make a context on `device` (which must be current) whose
+ * workspace serves fused_gemm_reduce calls with P <= max_P, M <= max_M and the
+ * given N and K: fp32 partials of max_P*max_M*N floats, band counters, the
+ * mxfp8 scale repack area and the fp8-wire staging.  Like the pages' window
+ * it is sized once and never grows (sglang pull request #40757, "Worth a
+ * reviewer's attention": the window is sized from the chunked-prefill
+ * ceiling, not from the first request).  wait_timeout_ns bounds every
+ * device-side wait (0 = 2 s).  Unless GEMMAR_NO_SELF_TEST is set, runs the
+ * fused path once on a closed-form case (unit codes and scales: every output
+ * equals P*K) under that deadline and fails with GEMMAR_ERR_DEVICE on a
+ * mismatch (the pages' self_test(), sglang pull request #40757).
+ * On success *out owns device memory until gemmar_destroy.
+ */
+int gemmar_create(gemmar_ctx **out, int device, int64_t max_M, int64_t N, int64_t K, int max_P,
+                  uint32_t flags, int64_t wait_timeout_ns);
+
+/* gemmar_destroy -- synchronise the context's device and free its workspace. */
+int gemmar_destroy(gemmar_ctx *ctx);
+
+/*
+ * gemmar_status -- read (blocking) the device status word; call after the
+ * work is complete.  Returns GEMMAR_OK or the first device-side error
+ * (GEMMAR_ERR_TIMEOUT); *detail (if not NULL) receives where it happened
+ * (see the kernels' wait-site codes).  A device error disables the context.
+ */
+int gemmar_status(gemmar_ctx *ctx, int *detail);
+
+/* gemmar_workspace_bytes -- device bytes the context holds. */
+int64_t gemmar_workspace_bytes(const gemmar_ctx *ctx);
+
+/*
+ * Phase timing of fused_gemm_reduce, the per-layer breakdown of the MORI
+ * page's "Where the time goes" table.  gemmar_set_phase_timing(ctx, 1) makes
+ * every later fused call record CUDA events on its stream between its kernel
+ * launches (nothing is skipped or reordered).  gemmar_phase_times waits for
+ * those events, writes the summed milliseconds of each phase over the
+ * recorded calls into ms[GEMMAR_NUM_PHASES] and the number of calls into
+ * *calls, and clears the record.  Phases: GEMMAR_PHASE_GEMM (scale repack,
+ * GEMM with band-ordered partial stores), GEMMAR_PHASE_REDUCE (band_reduce),
+ * GEMMAR_PHASE_QUANTIZE and GEMMAR_PHASE_DEQUANTIZE (the fp8 wire; 0 when off).
+ * At most 65536 calls are recorded between reads (later ones are not timed).
+ */
+enum { GEMMAR_PHASE_GEMM = 0, GEMMAR_PHASE_REDUCE = 1, GEMMAR_PHASE_QUANTIZE = 2,
+       GEMMAR_PHASE_DEQUANTIZE = 3, GEMMAR_NUM_PHASES = 4 };
+int gemmar_set_phase_timing(gemmar_ctx *ctx, int enable);
+int gemmar_phase_times(gemmar_ctx *ctx, float *ms, int *calls);
+
+/*
+ * gemm_blockscale_fp8 -- C[M,N] = A[M,K] * B[N,K]^T for one K-slice, with
+ *   C[m,n] = sum_kb (sa[m,kb]*sb[n/128,kb]) * sum_{k in kb} a[m,k]*b[n,k]
+ * accumulated in fp32 (tcgen05 MMA per 128-K block into TMEM, the scales
+ * applied while draining TMEM).  Blockscale quantisation as on the MORI page
+ * ("Running the benchmark": A 1x128, B 128x128, fp32 scales).
+ *   A: e4m3 [M,K]; sa: fp32 [M, K/128]; B: e4m3 [N,K]; sb: fp32 [N/128, K/128];
+ *   C: [M,N] of c_dtype (GEMMAR_DTYPE_F32 or GEMMAR_DTYPE_BF16, RNE).
+ * Shape rules as gemmar_supports with P = bands = 1.
+ */
+int gemm_blockscale_fp8(gemmar_ctx *ctx, const uint8_t *A, const float *sa, const uint8_t *B,
+                        const float *sb, void *C, int c_dtype, int64_t M, int64_t N, int64_t K,
+                        void *stream);
+
+/*
+ * gemm_mxfp8 -- C[M,N] = sum_g 2^(ea[m,g]+eb[n,g]-254) * sum_{k in g} a[m,k]*b[n,k]
+ * for one K-slice, on the native block-scaled MMA (tcgen05 kind::mxf8f6f4,
+ * one ue8m0 scale per 32 of K); the mxfp8 wo_b of sglang pull request #43480.
+ *   A: e4m3 [M,K]; ea: ue8m0 bytes [M, K/32]; B: e4m3 [N,K]; eb: [N, K/32];
+ *   C: [M,N] of c_dtype.  Uses the context's repack area (needs M <= max_M,
+ *   N and K <= those of gemmar_create, else GEMMAR_ERR_WORKSPACE).
+ */
+int gemm_mxfp8(gemmar_ctx *ctx, const uint8_t *A, const uint8_t *ea, const uint8_t *B,
+               const uint8_t *eb, void *C, int c_dtype, int64_t M, int64_t N, int64_t K,
+               void *stream);
+
+/*
+ * band_reduce -- the fixed-order reduce of the row-parallel layer: for band
+ * b (rows b*M/bands .. (b+1)*M/bands-1),
+ *   out[m,n] = bf16_rn( ((W[b][0][r][n] + W[b][1][r][n]) + ...) + W[b][P-1][r][n] )
+ * in fp32, p ascending ("MORI GEMM + All-Reduce Benchmark", "The fp8 wire":
+ * the reduce accumulates in fp32; "Negative results": the reduce streams
+ * through all source slices at once).  Bit-exact and deterministic.
+ *   W: fp32 [bands][P][M/bands][N] (caller-owned); out: bf16 [M,N].
+ */
+int band_reduce(gemmar_ctx *ctx, const float *W, int P, int64_t M, int64_t N, int bands,
+                uint16_t *out, void *stream);
+
+/*
+ * rowquant_e4m3 -- the fp8 wire's narrowing: per row m of x [M,N],
+ *   s[m] = fp32(amax_n |x[m,n]| / 448),  q[m,n] = e4m3_rn_sat(fp32(x[m,n] / s[m]))
+ * (IEEE division; a zero row gives s = 0 and +0 codes).  One fp32 scale per
+ * row ("MORI GEMM + All-Reduce Benchmark", "The fp8 wire"; sglang pull
+ * request #40757, "The optional fp8 gather").
+ *   x: [M,N] of x_dtype (GEMMAR_DTYPE_BF16 or GEMMAR_DTYPE_F32); q: uint8 [M,N];
+ *   row_scale: fp32 [M].  N % 16 == 0.  Bit-exact against the definition.
+ */
+int rowquant_e4m3(gemmar_ctx *ctx, const void *x, int x_dtype, int64_t M, int64_t N,
+                  uint8_t *q, float *row_scale, void *stream);
+
+/*
+ * rowdequant_e4m3 -- the fp8 wire's widening: y[m,n] = bf16_rn(fp32(decode(q[m,n]) * s[m]))
+ * ("MORI GEMM + All-Reduce Benchmark", "Who moves the gather": the second
+ * kernel that widens the landed fp8).
+ *   q: uint8 [M,N]; row_scale: fp32 [M]; y: bf16 [M,N].  N % 16 == 0.
+ */
+int rowdequant_e4m3(gemmar_ctx *ctx, const uint8_t *q, const float *row_scale, int64_t M,
+                    int64_t N, uint16_t *y, void *stream);
+
+/*
+ * quant_blockscale_e4m3 -- device quantiser for blockscale operands: groups
+ * of group_rows x 128 (group_rows 1 for activations, 128 for weights) of an
+ * fp32 [R,C] matrix; s = fp32(amax/448), q = e4m3_rn_sat(fp32(x/s)); a zero
+ * group gives s = 0 and +0 codes.  The real call site quantises wo_b's bf16
+ * input itself (sglang pull request #43480, "Numerics, measured where the
+ * path engages").  q: uint8 [R,C]; scales: fp32 [ceil(R/group_rows), C/128].
+ * C % 128 == 0.  Bit-exact against the definition.
+ */
+int quant_blockscale_e4m3(gemmar_ctx *ctx, const float *x, int64_t R, int64_t C, int group_rows,
+                          uint8_t *q, float *scales, void *stream);
+
+/*
+ * quant_mx_e4m3 -- device mxfp8 quantiser: per 1x32 group of an fp32 [R,C]
+ * matrix, byte = ceil(log2(fp32(amax/448))) + 127 from the IEEE bits (exact at
+ * powers of two; sglang pull request #43480, review item 7), clamped to
+ * [0,254], 0 for a zero group; q = e4m3_rn_sat(fp32(x * 2^(127-byte))).
+ * q: uint8 [R,C]; e8m0: uint8 [R, C/32].  C % 32 == 0.  Bit-exact.
+ */
+int quant_mx_e4m3(gemmar_ctx *ctx, const float *x, int64_t R, int64_t C, uint8_t *q,
+                  uint8_t *e8m0, void *stream);
+
+/*
+ * fused_gemm_reduce -- the whole wo_b path for P K-slices resident on this
+ * GPU: one persistent GEMM launch over every (band, slice, tile) in band
+ * order whose epilogue stores each tile's fp32 partial into the context's
+ * workspace W[band][p] and signals that band's counter as soon as the tile
+ * retires (sglang pull request #40757, "What": the fused kernel hands each
+ * row band over as soon as that band's tiles are done); then band_reduce
+ * waits (bounded) for each band's counter and sums the P partials in fixed
+ * order to bf16 out [M,N].  With GEMMAR_FP8_WIRE the reduced rows then go
+ * through rowquant_e4m3 + rowdequant_e4m3 ("The fp8 wire").
+ *   A[p], B[p], sa[p], sb[p]: HOST arrays of P device pointers; per slice as in
+ *   gemm_blockscale_fp8 (scale_kind GEMMAR_SCALE_BLOCK128) or gemm_mxfp8
+ *   (GEMMAR_SCALE_MX32).  bands: row bands (0 = P).  out: bf16 [M,N].
+ * Deterministic: equal, bit for bit, to P x gemm_*(F32) into W followed by
+ * band_reduce, and to itself on a rerun.
+ */
+int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A, const void *const *sa,
+                      const uint8_t *const *B, const void *const *sb, int scale_kind,
+                      int64_t M, int64_t N, int64_t K, int bands, uint32_t flags,
+                      uint16_t *out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMMAR_H */

@@ -1,0 +1,51 @@
+"""Shared helpers for the parity tests: seeded operands (drawn by `synthetic`,
+quantised by the oracle on the host, so both sides consume identical codes and
+scales) and the tolerance checks written in the tests."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synthetic
+
+# the bf16 GEMM+reduce tolerance against the fp64 oracle
+REL_L2_MAX = 4e-3
+ELEM_REL = 1e-2
+ELEM_ABS = 1e-3
+
+
+def blockscale_operands(P, M, N, K, seed=0):
+    A, sa, B, sb = [], [], [], []
+    for p in range(P):
+        a, s = oracle.quant_act_1x128(synthetic.normal(seed, synthetic.TID_A, p, (M, K)))
+        b, t = oracle.quant_weight_128x128(synthetic.normal(seed, synthetic.TID_B, p, (N, K), sigma=0.02))
+        A.append(a); sa.append(s); B.append(b); sb.append(t)
+    return A, sa, B, sb
+
+
+def mx_operands(P, M, N, K, seed=0):
+    A, sa, B, sb = [], [], [], []
+    for p in range(P):
+        a, s = oracle.quant_mx(synthetic.normal(seed, synthetic.TID_A, p, (M, K)))
+        b, t = oracle.quant_mx(synthetic.normal(seed, synthetic.TID_B, p, (N, K), sigma=0.02))
+        A.append(a); sa.append(s); B.append(b); sb.append(t)
+    return A, sa, B, sb
+
+
+def rel_l2(x, ref):
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    return float(np.linalg.norm((x - ref).ravel()) / max(np.linalg.norm(ref.ravel()), 1e-300))
+
+
+def check_bf16_output(got, ref, what=""):
+    """relL2 <= 4e-3 and |err| <= 1e-2 |ref| + 1e-3 elementwise (fp64 reference)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite outputs (unwritten tiles?)"
+    rl = rel_l2(got, ref)
+    err = np.abs(got - ref)
+    bad = err > ELEM_REL * np.abs(ref) + ELEM_ABS
+    assert rl <= REL_L2_MAX, f"{what}: relL2 {rl:.3e} > {REL_L2_MAX}"
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements out of bound, worst {err[bad].max():.3e}"
+    return rl

@@ -1,0 +1,66 @@
+"""The C-ABI library loads and exports every entry point include/gemmar.h
+declares; the host-only shape check answers without a GPU (CPU only: no
+compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemmar.h")
+LIB = os.path.join(ROOT, "block_scaled_fp8_gemm_gb300", "libgemmar.so")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:int|int64_t|void)\s+\**\s*([a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        import __graft_entry__
+        __graft_entry__.build()
+    return ctypes.CDLL(LIB)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("gemmar_create", "gemmar_destroy", "gemmar_status", "gemm_blockscale_fp8", "gemm_mxfp8",
+                     "band_reduce", "rowquant_e4m3", "rowdequant_e4m3", "fused_gemm_reduce"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_binding_covers_every_declared_symbol(lib):
+    import block_scaled_fp8_gemm_gb300 as g
+    assert sorted(g.EXPORTED) == declared_functions()
+    for n in declared_functions():
+        assert callable(getattr(g, n))
+
+
+def test_shape_rules_host_only(lib):
+    sup = lib.gemmar_supports
+    sup.restype = ctypes.c_int
+    sup.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int]
+    OK, ARG, SHAPE = 0, 1, 2
+    assert sup(8, 16384, 7168, 2048, 8, 0) == OK        # the headline shape
+    assert sup(4, 16384, 7168, 2048, 4, 1) == OK        # the mxfp8 shape
+    assert sup(2, 256, 512, 256, 2, 0) == OK            # the tiny shape
+    assert sup(8, 604, 7168, 2048, 8, 0) == SHAPE       # M not a multiple of the band count
+    assert sup(8, 600, 7168, 2048, 8, 0) == OK          # ragged bands: 75 rows each
+    assert sup(1, 200, 384, 256, 1, 0) == OK            # ragged M (one band)
+    assert sup(1, 128, 7200, 2048, 1, 0) == SHAPE       # N off the 128 grid
+    assert sup(1, 128, 448, 2048, 1, 0) == SHAPE        # blockscale N needs the 128 grid
+    assert sup(1, 128, 448, 2048, 1, 1) == OK           # mx N may use the 224 tile
+    assert sup(1, 128, 7168, 2000, 1, 0) == SHAPE       # K off the 128 grid
+    assert sup(9, 128, 256, 128, 1, 0) == ARG           # more slices than the ABI takes
+    assert sup(2, 128, 256, 128, 0, 0) == ARG
+    assert sup(2, 128, 256, 128, 2, 7) == ARG           # unknown scale kind

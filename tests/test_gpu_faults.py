@@ -1,0 +1,77 @@
+"""Failure handling through the C ABI, without faulting the GPU: argument,
+shape, alignment and workspace errors return at once and launch nothing; a
+band that is never signalled (host-set fault flag) makes the reducer's bounded
+wait expire, which the status word reports and which disables the context;
+the closed-form self-test passes at create time."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import blockscale_operands
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def g():
+    import block_scaled_fp8_gemm_gb300 as g
+    return g
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def test_create_runs_closed_form_self_test(g):
+    torch.cuda.set_device(0)
+    ctx = g.gemmar_create(0, 512, 512, 256, 2)        # self-test on (blockscale and mx)
+    assert g.gemmar_workspace_bytes(ctx) >= 2 * 512 * 512 * 4
+    assert g.gemmar_status(ctx) == (0, 0)
+    ctx.close()
+
+
+def test_host_side_errors_launch_nothing(g):
+    torch.cuda.set_device(0)
+    ctx = g.gemmar_create(0, 256, 512, 256, 2, flags=g.GEMMAR_NO_SELF_TEST)
+    A, sa, B, sb = blockscale_operands(2, 256, 512, 256, seed=1)
+    dA, dsa, dB, dsb = [dev(a) for a in A], [dev(s) for s in sa], [dev(b) for b in B], [dev(s) for s in sb]
+    out = torch.empty((256, 512), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(g.GemmarError) as e:     # M not a multiple of the band count
+        g.fused_gemm_reduce(ctx, dA, dsa, dB, dsb, out, bands=3)
+    assert e.value.code == g.GEMMAR_ERR_SHAPE
+    big = [torch.zeros((512, 256), dtype=torch.uint8, device="cuda")] * 2
+    bigs = [torch.ones((512, 2), dtype=torch.float32, device="cuda")] * 2
+    out2 = torch.empty((512, 512), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(g.GemmarError) as e:     # more rows than the workspace was sized for
+        g.fused_gemm_reduce(ctx, big, bigs, dB, dsb, out2)
+    assert e.value.code == g.GEMMAR_ERR_WORKSPACE
+    raw = torch.empty(256 * 512 * 2 + 16, dtype=torch.uint8, device="cuda")
+    misaligned = raw[8:8 + 256 * 512 * 2].view(torch.bfloat16).view(256, 512)
+    with pytest.raises(g.GemmarError) as e:
+        g.fused_gemm_reduce(ctx, dA, dsa, dB, dsb, misaligned)
+    assert e.value.code == g.GEMMAR_ERR_ALIGN
+    torch.cuda.synchronize()
+    assert g.gemmar_status(ctx)[0] == 0
+    ctx.close()
+
+
+def test_unsignalled_band_times_out_cleanly(g):
+    torch.cuda.set_device(0)
+    ctx = g.gemmar_create(0, 256, 512, 256, 2, flags=g.GEMMAR_NO_SELF_TEST, wait_timeout_ns=50_000_000)
+    A, sa, B, sb = blockscale_operands(2, 256, 512, 256, seed=2)
+    dA, dsa, dB, dsb = [dev(a) for a in A], [dev(s) for s in sa], [dev(b) for b in B], [dev(s) for s in sb]
+    out = torch.empty((256, 512), dtype=torch.bfloat16, device="cuda")
+    g.fused_gemm_reduce(ctx, dA, dsa, dB, dsb, out, flags=g.GEMMAR_FAULT_SKIP_BAND)
+    torch.cuda.synchronize()                    # the wait gave up: no hang, context still usable
+    code, detail = g.gemmar_status(ctx)
+    assert code == g.GEMMAR_ERR_TIMEOUT and detail == 7      # the reducer's band wait
+    with pytest.raises(g.GemmarError) as e:     # sticky-disabled afterwards
+        g.fused_gemm_reduce(ctx, dA, dsa, dB, dsb, out)
+    assert e.value.code == g.GEMMAR_ERR_DISABLED
+    ctx.close()
+    # a fresh context on the same device works
+    ctx2 = g.gemmar_create(0, 256, 512, 256, 2, flags=g.GEMMAR_NO_SELF_TEST)
+    g.fused_gemm_reduce(ctx2, dA, dsa, dB, dsb, out)
+    torch.cuda.synchronize()
+    assert g.gemmar_status(ctx2)[0] == 0
+    ctx2.close()

@@ -1,0 +1,173 @@
+"""GPU parity of the tcgen05 GEMMs and the fused GEMM + band reduce against the
+fp64 oracle, through the C ABI, at sizes that span several tiles and ragged
+tails; plus the fused path's determinism and its bitwise equality with the
+split path (GEMM per slice into fp32 partials, then band_reduce)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import blockscale_operands, check_bf16_output, mx_operands, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def g():
+    import block_scaled_fp8_gemm_gb300 as g
+    return g
+
+
+@pytest.fixture(scope="module")
+def ctx(g):
+    torch.cuda.set_device(0)
+    c = g.gemmar_create(0, 1024, 1024, 512, 8, flags=g.GEMMAR_NO_SELF_TEST, wait_timeout_ns=1_000_000_000)
+    yield c
+    c.close()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def u16(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def status_ok(g, ctx):
+    torch.cuda.synchronize()
+    code, detail = g.gemmar_status(ctx)
+    assert code == 0, f"device status {code} at site {detail}"
+
+
+def check_f32_output(got, ref, what):
+    # fp32 accumulation and promotion against fp64: a few fp32 roundings of the
+    # magnitudes involved
+    got = np.asarray(got, np.float64)
+    scale = np.sqrt(np.mean(ref ** 2))
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)), what
+    assert rel_l2(got, ref) <= 2e-6, (what, rel_l2(got, ref))
+    assert np.all(err <= 1e-5 * np.abs(ref) + 2e-5 * scale), (what, err.max())
+
+
+# ------------------------------------------------------------ single-slice GEMMs
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (256, 512, 256), (200, 384, 512), (384, 768, 384),
+                                   (64, 256, 256), (1, 128, 128)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_gemm_blockscale(g, ctx, M, N, K, out_dtype):
+    A, sa, B, sb = blockscale_operands(1, M, N, K, seed=M + N + K)
+    ref, ref16 = oracle.gemm_reduce(A, sa, B, sb, 0)
+    C = torch.full((M, N), float("nan"), dtype=out_dtype, device="cuda")
+    g.gemm_blockscale_fp8(ctx, dev(A[0]), dev(sa[0]), dev(B[0]), dev(sb[0]), C)
+    status_ok(g, ctx)
+    if out_dtype == torch.float32:
+        check_f32_output(C.cpu().numpy(), ref, f"blockscale f32 {M}x{N}x{K}")
+    else:
+        check_bf16_output(C.float().cpu().numpy(), ref, f"blockscale bf16 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (256, 448, 256), (200, 384, 512), (128, 896, 128),
+                                   (1, 128, 256)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_gemm_mxfp8(g, ctx, M, N, K, out_dtype):
+    A, ea, B, eb = mx_operands(1, M, N, K, seed=M + N + K)
+    ref, _ = oracle.gemm_reduce(A, ea, B, eb, 1)
+    C = torch.full((M, N), float("nan"), dtype=out_dtype, device="cuda")
+    g.gemm_mxfp8(ctx, dev(A[0]), dev(ea[0]), dev(B[0]), dev(eb[0]), C)
+    status_ok(g, ctx)
+    if out_dtype == torch.float32:
+        check_f32_output(C.cpu().numpy(), ref, f"mx f32 {M}x{N}x{K}")
+    else:
+        check_bf16_output(C.float().cpu().numpy(), ref, f"mx bf16 {M}x{N}x{K}")
+
+
+def test_gemm_zero_scale_rows_and_blocks(g, ctx):
+    M, N, K = 256, 512, 256
+    A, sa, B, sb = blockscale_operands(1, M, N, K, seed=77)
+    sa[0][5, :] = 0.0          # a zero row: exact zeros
+    sb[0][2, :] = 0.0          # B block-row 2: columns 256..383 exactly zero
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, 0)
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    g.gemm_blockscale_fp8(ctx, dev(A[0]), dev(sa[0]), dev(B[0]), dev(sb[0]), C)
+    status_ok(g, ctx)
+    c = C.cpu().numpy()
+    assert np.all(c[5] == 0) and np.all(c[:, 256:384] == 0)
+    check_f32_output(c, ref, "zero scales")
+
+
+# ------------------------------------------------------------ fused GEMM + reduce
+
+def run_fused(g, ctx, A, sa, B, sb, kind, bands, flags=0):
+    M, N = A[0].shape[0], B[0].shape[0]
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    g.fused_gemm_reduce(ctx, [dev(a) for a in A], [dev(s) for s in sa], [dev(b) for b in B],
+                        [dev(s) for s in sb], out, scale_kind=kind, bands=bands, flags=flags)
+    status_ok(g, ctx)
+    return out
+
+
+@pytest.mark.parametrize("P,M,N,K,bands", [(2, 256, 512, 256, 2),      # the tiny configuration
+                                           (4, 512, 768, 256, 4),
+                                           (3, 600, 384, 384, 3),      # ragged bands (200 rows)
+                                           (8, 1024, 256, 128, 8),
+                                           (2, 256, 512, 256, 1)])
+def test_fused_blockscale_vs_oracle(g, ctx, P, M, N, K, bands):
+    A, sa, B, sb = blockscale_operands(P, M, N, K, seed=P * M)
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, 0)
+    out = run_fused(g, ctx, A, sa, B, sb, g.GEMMAR_SCALE_BLOCK128, bands, flags=g.GEMMAR_DEBUG_CANARY)
+    rl = check_bf16_output(out.float().cpu().numpy(), ref, f"fused P={P} M={M} N={N} K={K} bands={bands}")
+    assert rl < 2.35e-3      # fp32 partials stay below the pages' bf16-partial level
+
+
+@pytest.mark.parametrize("P,M,N,K,bands", [(2, 256, 448, 256, 2), (4, 384, 256, 128, 4), (3, 600, 384, 256, 3)])
+def test_fused_mx_vs_oracle(g, ctx, P, M, N, K, bands):
+    A, ea, B, eb = mx_operands(P, M, N, K, seed=P * M + 1)
+    ref, _ = oracle.gemm_reduce(A, ea, B, eb, 1)
+    out = run_fused(g, ctx, A, ea, B, eb, g.GEMMAR_SCALE_MX32, bands, flags=g.GEMMAR_DEBUG_CANARY)
+    check_bf16_output(out.float().cpu().numpy(), ref, f"fused mx P={P} M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+def test_fused_equals_split_bitwise_and_is_deterministic(g, ctx, kind):
+    P, M, N, K, bands = 4, 512, 512, 256, 4
+    ops = blockscale_operands(P, M, N, K, seed=5) if kind == 0 else mx_operands(P, M, N, K, seed=5)
+    A, sa, B, sb = ops
+    out1 = run_fused(g, ctx, A, sa, B, sb, kind, bands)
+    out2 = run_fused(g, ctx, A, sa, B, sb, kind, bands)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16)), "fused run is not deterministic"
+    # split path: each slice's fp32 GEMM, arranged as W[band][p], then band_reduce
+    rpb = M // bands
+    W = torch.empty((bands, P, rpb, N), dtype=torch.float32, device="cuda")
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    gemm = g.gemm_blockscale_fp8 if kind == 0 else g.gemm_mxfp8
+    for p in range(P):
+        gemm(ctx, dev(A[p]), dev(sa[p]), dev(B[p]), dev(sb[p]), C)
+        W[:, p] = C.view(bands, rpb, N)
+    split = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    g.band_reduce(ctx, W, P, M, N, bands, split)
+    status_ok(g, ctx)
+    assert torch.equal(out1.view(torch.int16), split.view(torch.int16)), "fused != split"
+
+
+def test_fused_fp8_wire(g, ctx):
+    P, M, N, K = 2, 256, 512, 256
+    A, sa, B, sb = blockscale_operands(P, M, N, K, seed=9)
+    ref, ref16 = oracle.gemm_reduce(A, sa, B, sb, 0)
+    plain = run_fused(g, ctx, A, sa, B, sb, 0, P)
+    wire = run_fused(g, ctx, A, sa, B, sb, 0, P, flags=g.GEMMAR_FP8_WIRE)
+    # against the oracle's own chain: fp64 sum -> bf16 -> per-row e4m3 codec
+    q_ref, s_ref = oracle.rowquant(oracle.bf16_to_f32(ref16))
+    wire_ref = oracle.bf16_to_f32(oracle.rowdequant(q_ref, s_ref))
+    w = wire.float().cpu().numpy()
+    assert rel_l2(w, ref) <= 3e-2
+    assert rel_l2(w, wire_ref) <= 1e-2
+    # the wire is exactly the GPU codec applied to the GPU's reduced rows
+    q = torch.empty((M, N), dtype=torch.uint8, device="cuda")
+    s = torch.empty((M,), dtype=torch.float32, device="cuda")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    g.rowquant_e4m3(ctx, plain, q, s)
+    g.rowdequant_e4m3(ctx, q, s, y)
+    status_ok(g, ctx)
+    assert torch.equal(y.view(torch.int16), wire.view(torch.int16))

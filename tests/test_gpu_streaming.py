@@ -1,0 +1,156 @@
+"""GPU parity of the streaming kernels against the oracle, through the C ABI:
+the per-row e4m3 codec (bit-exact), the device quantisers (bit-exact) and the
+fixed-order band reduce (bit-exact against the ordered fp32 definition, and
+within tolerance of the fp64 oracle)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from helpers import check_bf16_output, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+TABLE = oracle.e4m3_decode_table()
+
+
+@pytest.fixture(scope="module")
+def g():
+    import block_scaled_fp8_gemm_gb300 as g
+    return g
+
+
+@pytest.fixture(scope="module")
+def ctx(g):
+    torch.cuda.set_device(0)
+    c = g.gemmar_create(0, 512, 256, 128, 2, flags=g.GEMMAR_NO_SELF_TEST, wait_timeout_ns=500_000_000)
+    yield c
+    c.close()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def u16(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def assert_status_ok(g, ctx):
+    torch.cuda.synchronize()
+    code, detail = g.gemmar_status(ctx)
+    assert code == 0, (code, detail)
+
+
+# ---------------------------------------------------------------- row codec
+
+def codec_gpu(g, ctx, x_t):
+    M, N = x_t.shape
+    q = torch.empty((M, N), dtype=torch.uint8, device="cuda")
+    s = torch.empty((M,), dtype=torch.float32, device="cuda")
+    g.rowquant_e4m3(ctx, x_t, q, s)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    g.rowdequant_e4m3(ctx, q, s, y)
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), s.cpu().numpy(), u16(y)
+
+
+def test_rowcodec_bitexact_fp32_page_payload(g, ctx):
+    # the page's payload shape: [2048, 7168] standard normal, fed as identical fp32 rows
+    x = synthetic.normal(0, synthetic.TID_X, 0, (2048, 7168))
+    q, s, y = codec_gpu(g, ctx, dev(x))
+    q_ref, s_ref = oracle.rowquant(x)
+    assert np.array_equal(s, s_ref)
+    assert np.array_equal(q, q_ref)
+    assert np.array_equal(y, oracle.rowdequant(q_ref, s_ref))
+    err = rel_l2(oracle.bf16_to_f32(y), x)
+    assert abs(err - 2.646e-2) < 0.01 * 2.646e-2      # the page's per-row figure
+
+
+def test_rowcodec_bitexact_bf16_rows(g, ctx):
+    x32 = synthetic.normal(1, synthetic.TID_X, 1, (333, 7168), sigma=3.0)
+    xb = torch.from_numpy(x32).to(torch.bfloat16)
+    x_exact = xb.to(torch.float32).numpy()             # bf16 -> fp32 is exact
+    q, s, y = codec_gpu(g, ctx, xb.cuda())
+    q_ref, s_ref = oracle.rowquant(x_exact)
+    assert np.array_equal(s, s_ref) and np.array_equal(q, q_ref)
+    assert np.array_equal(y, oracle.rowdequant(q_ref, s_ref))
+
+
+def test_rowcodec_edge_cases(g, ctx):
+    x = synthetic.normal(2, synthetic.TID_X, 2, (8, 256))
+    x[0] = 0.0                                       # zero row
+    x[1] = -0.0                                      # negative-zero row
+    x[2, 5] = 448.0 * 16                             # amax a power of two of 448
+    x[3] = np.float32(2.0 ** -118) * x[3]            # tiny row (subnormal codes)
+    x[4, ::2] = 0.0                                  # zeros inside a row
+    x[5] *= np.float32(1e30)                         # huge row
+    x[6, 100] = -x[6].__abs__().max() * 2            # negative amax
+    for M in (8, 3, 1):                              # ragged row counts
+        q, s, y = codec_gpu(g, ctx, dev(x[:M]))
+        q_ref, s_ref = oracle.rowquant(x[:M])
+        assert np.array_equal(s, s_ref) and np.array_equal(q, q_ref)
+        assert np.array_equal(y, oracle.rowdequant(q_ref, s_ref))
+
+
+def test_rowdequant_all_codes(g, ctx):
+    codes = np.arange(256, dtype=np.uint8)
+    codes[codes == 0x7F] = 0x7E
+    codes[codes == 0xFF] = 0xFE
+    q = np.tile(codes, (6, 1))
+    s = np.array([1.0, 0.5, 3.0, 1e-30, 7e30, 0.0], dtype=np.float32)
+    y = torch.empty((6, 256), dtype=torch.bfloat16, device="cuda")
+    g.rowdequant_e4m3(ctx, dev(q), dev(s), y)
+    torch.cuda.synchronize()
+    assert np.array_equal(u16(y), oracle.rowdequant(q, s))
+
+
+# ---------------------------------------------------------------- quantisers
+
+@pytest.mark.parametrize("R,C,gr", [(256, 512, 1), (77, 384, 1), (256, 512, 128), (300, 256, 128)])
+def test_quant_blockscale_bitexact(g, ctx, R, C, gr):
+    x = synthetic.normal(3, synthetic.TID_A, R, (R, C), sigma=0.02 if gr == 128 else 1.0)
+    x[0, :128] = 0.0
+    q = torch.empty((R, C), dtype=torch.uint8, device="cuda")
+    s = torch.empty(((R + gr - 1) // gr, C // 128), dtype=torch.float32, device="cuda")
+    g.quant_blockscale_e4m3(ctx, dev(x), gr, q, s)
+    torch.cuda.synchronize()
+    q_ref, s_ref = oracle.quant_block(x, gr, 128)
+    assert np.array_equal(s.cpu().numpy(), s_ref)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+
+
+@pytest.mark.parametrize("R,C", [(128, 256), (37, 96)])
+def test_quant_mx_bitexact(g, ctx, R, C):
+    x = synthetic.normal(4, synthetic.TID_A, R, (R, C))
+    x[1, 32:64] = 0.0
+    x[2, 0:32] = np.float32(448.0 * 2.0 ** -5)       # a group on an exact power of two of 448
+    x[3, 64:96] *= np.float32(2.0 ** -100)
+    q = torch.empty((R, C), dtype=torch.uint8, device="cuda")
+    e = torch.empty((R, C // 32), dtype=torch.uint8, device="cuda")
+    g.quant_mx_e4m3(ctx, dev(x), q, e)
+    torch.cuda.synchronize()
+    q_ref, e_ref = oracle.quant_mx(x)
+    assert np.array_equal(e.cpu().numpy(), e_ref)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+
+
+# ---------------------------------------------------------------- band reduce
+
+@pytest.mark.parametrize("P,M,N,bands", [(2, 256, 512, 2), (8, 512, 256, 8), (1, 128, 128, 1),
+                                         (3, 96, 384, 3), (5, 40, 128, 5), (8, 512, 256, 1)])
+def test_band_reduce_bitexact(g, ctx, P, M, N, bands):
+    rpb = M // bands
+    W = synthetic.normal(5, synthetic.TID_W, P, (bands, P, rpb, N))
+    W[..., 0] = np.float32(1e-30)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    g.band_reduce(ctx, dev(W), P, M, N, bands, out)
+    torch.cuda.synchronize()
+    got = u16(out)
+    for b in range(bands):
+        ref = oracle.reduce_f32_ordered(W[b])
+        assert np.array_equal(got[b * rpb:(b + 1) * rpb], ref), f"band {b}"
+    # and within the tolerance of the fp64 sum
+    exact = W.astype(np.float64).sum(axis=1).reshape(M, N)
+    check_bf16_output(oracle.bf16_to_f32(got), exact, "band_reduce vs fp64")
