@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                     const uint32_t sf = smem_u32(smem + C::kOffSf + stage * C::kSfBytes);
                     tc_cp_32x128b_warpx4(sfa_t, smem_desc(sf, 0, 128, 0));
                     tc_cp_32x128b_warpx4(sfb_t, smem_desc(sf + 512, 0, 128, 0));
-                    tc_cp_32x128b_warpx4(sfb_t + 4, smem_desc(sf + 768, 0, 128, 0));
+                    tc_cp_32x128b_warpx4(sfb_t + 4, smem_desc(sf + 1024, 0, 128, 0));
                     const uint64_t ad = desc_kmajor_sw128(smem_u32(smem + C::kOffA + stage * C::kABytes));
                     const uint64_t bd = desc_kmajor_sw128(smem_u32(smem + C::kOffB + stage * C::kBBytes));
 #pragma unroll
