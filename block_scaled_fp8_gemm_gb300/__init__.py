@@ -51,6 +51,7 @@ GEMMAR_DEBUG_CANARY = 1 << 1
 GEMMAR_FAULT_SKIP_BAND = 1 << 2
 GEMMAR_NO_SELF_TEST = 1 << 3
 GEMMAR_MAX_P = 8
+GEMMAR_NOALLOC_MAX_PARTIALS = 8 * 1024 * 1024
 
 # ---- signatures ----------------------------------------------------------------
 _P = ctypes.c_void_p
@@ -75,6 +76,7 @@ _SIGS = {
     "quant_blockscale_e4m3": (_I, [_P, _P, _I64, _I64, _I, _P, _P, _P]),
     "quant_mx_e4m3": (_I, [_P, _P, _I64, _I64, _P, _P, _P]),
     "fused_gemm_reduce": (_I, [_P, _I, _PP, _PP, _PP, _PP, _I, _I64, _I64, _I64, _I, _U32, _P, _P]),
+    "fused_gemm_reduce_noalloc": (_I, [_I, _PP, _PP, _PP, _PP, _I64, _I64, _I64, _I, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -287,3 +289,21 @@ def fused_gemm_reduce(ctx: Context, A: Sequence, sa: Sequence, B: Sequence, sb: 
     _check(_lib.fused_gemm_reduce(ctx.handle, P, cast(pa), cast(psa), cast(pb), cast(psb), scale_kind,
                                   M, N, K, bands, flags, _bf16(out, "out"), _stream(stream)),
            "fused_gemm_reduce")
+
+
+def fused_gemm_reduce_noalloc(A: Sequence, sa: Sequence, B: Sequence, sb: Sequence, out, bands: int = 0,
+                              stream=None) -> None:
+    """Blockscale fused GEMM + band reduce that allocates no device memory
+    (its scratch is fixed-size library memory, at most
+    GEMMAR_NOALLOC_MAX_PARTIALS fp32 partials).  For callers that cannot call
+    cudaMalloc, e.g. engines owning all device memory in a pool of their own."""
+    P = len(A)
+    if not (len(sa) == len(B) == len(sb) == P):
+        raise ValueError("A, sa, B, sb must have one entry per slice")
+    M, K = A[0].shape
+    N = B[0].shape[0]
+    arr = lambda ptrs: ctypes.cast((ctypes.c_void_p * P)(*ptrs), _PP)
+    _check(_lib.fused_gemm_reduce_noalloc(P, arr([_u8(a, "A[p]") for a in A]), arr([_f32(s, "sa[p]") for s in sa]),
+                                          arr([_u8(b, "B[p]") for b in B]), arr([_f32(s, "sb[p]") for s in sb]),
+                                          M, N, K, bands, _bf16(out, "out"), _stream(stream)),
+           "fused_gemm_reduce_noalloc")

@@ -246,6 +246,45 @@ int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A, const voi
                       int64_t M, int64_t N, int64_t K, int bands, uint32_t flags,
                       uint16_t *out, void *stream);
 
+/*
+ * fused_gemm_reduce_noalloc -- the blockscale fused_gemm_reduce for callers
+ * that cannot allocate device memory.  The pages have no counterpart; it is
+ * an addition of this library.
+ *
+ * Who needs it: an inference engine that takes all of the GPU's memory for
+ * its own pool at start-up and allows no cudaMalloc afterwards (a late
+ * allocation would fail or split its arena), or a host application that
+ * loads this library as a plugin and wants every device byte to come from its
+ * own allocator.  Neither can call gemmar_create, which allocates.  This call
+ * takes no context and allocates nothing (no cudaMalloc, no cudaFree, no
+ * allocating library routine): its scratch -- fp32 partials for up to
+ * GEMMAR_NOALLOC_MAX_PARTIALS elements (P*M*N), 1024 band counters and a
+ * status word -- lives in fixed-size arrays in the library's device code,
+ * which the CUDA driver reserves on every GPU that loads the library (32 MiB
+ * plus a few KiB per GPU) and keeps until the process exits.
+ *
+ * Arguments as fused_gemm_reduce with scale_kind GEMMAR_SCALE_BLOCK128 and no
+ * flags: A, sa, B, sb are HOST arrays of P device pointers, out is bf16 [M,N]
+ * on the current device, bands 0 means P.  Returns GEMMAR_ERR_WORKSPACE when
+ * P*M*N exceeds GEMMAR_NOALLOC_MAX_PARTIALS (use fused_gemm_reduce then), and
+ * the other codes as fused_gemm_reduce.  The result equals fused_gemm_reduce's
+ * bit for bit (same kernels, same fixed-order reduce).
+ *
+ * The first call on a device looks up the scratch's device addresses (and the
+ * driver loads the device code there); make that first call before any
+ * stream capture.  Every call on a device shares the one scratch, which keeps
+ * the last call's contents; the call clears its counters and status word
+ * itself.  Calls whose work overlaps on the GPU (different streams without an
+ * ordering between them, or several host threads) race on the scratch and
+ * give wrong results: keep them stream-ordered.  There is no status read-back:
+ * a device-side wait that expires (possible only if the GEMM launch itself
+ * failed) leaves `out` incomplete.
+ */
+#define GEMMAR_NOALLOC_MAX_PARTIALS (8 * 1024 * 1024)
+int fused_gemm_reduce_noalloc(int P, const uint8_t *const *A, const float *const *sa,
+                              const uint8_t *const *B, const float *const *sb,
+                              int64_t M, int64_t N, int64_t K, int bands, uint16_t *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
