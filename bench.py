@@ -152,7 +152,7 @@ def time_oracle(sample):
 
 def cpu_baseline_leg():
     import oracle
-    rpb, ncols = 128, 3584
+    rpb, ncols = 256, 7168           # 2048 rows x all columns: ~5e11 flop, 10-20 s on 16 cores
     sample = oracle_sample(rpb, ncols)
     dt, fl = time_oracle(sample)
     tflops = fl / dt / 1e12
@@ -166,7 +166,12 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     import oracle
-    rpb, ncols = 32, 1792
+    # size each step's sample so that warmup + steps take about two minutes:
+    # calibrate on a small sample, then scale the rows per band
+    ncols = 1792
+    t_cal, fl_cal = time_oracle(oracle_sample(8, ncols))
+    per_step = min(3.0, max(0.2, 120.0 / max(1, args.steps + args.warmup)))
+    rpb = int(max(1, min(M_HEAD // P_HEAD, round(8 * per_step / max(t_cal, 1e-3)))))
     sample = oracle_sample(rpb, ncols)
     for _ in range(max(args.warmup, 0)):
         time_oracle(sample)

@@ -176,8 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
         setmaxnreg_inc<kRegsHigh>();
         // ---------------------------------------------------- epilogue
         constexpr int HALF = BN / 2;
-        constexpr int NCH = HALF / 32;   // 32-column chunks per thread (even)
-        static_assert(NCH % 2 == 0, "chunk pipeline works in pairs");
+        constexpr int NCH = HALF / 32;   // 32-column store chunks per thread
+        static_assert(HALF % 64 == 0, "promotion works in 64-column TMEM loads");
         const int ew = warp - 4;        // 0..7
         const int q = warp & 3;         // TMEM lane quarter this warp may access
         const int h = ew >> 2;          // column half of the tile
@@ -207,30 +207,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
                 }
                 tc_fence_after();
                 const uint32_t taddr = lane_base + buf * BN;
-                uint32_t ra[32], rb[32];
-                tmem_ld_x32(taddr, ra);
-                tmem_wait_ld(ra);
+                // 64 columns per TMEM load: the buffer is free again after
+                // HALF/64 load round trips, before the last 64 promotions.
+                uint32_t r[64];
 #pragma unroll
-                for (int c = 0; c < NCH; c += 2) {
-                    tmem_ld_x32(taddr + (c + 1) * 32, rb);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        acc[c * 32 + j] = fmaf(s, __uint_as_float(ra[j]), acc[c * 32 + j]);
-                    tmem_wait_ld(rb);
-                    if (c + 2 >= NCH) {
-                        // whole K-block read: hand the buffer back to the MMA warp
+                for (int c = 0; c < HALF / 64; ++c) {
+                    tmem_ld_x64(taddr + c * 64, r);
+                    tmem_wait_ld(r);
+                    if (c == HALF / 64 - 1) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0)
                             mbar_arrive(tempty + buf);
-                    } else {
-                        tmem_ld_x32(taddr + (c + 2) * 32, ra);
                     }
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        acc[(c + 1) * 32 + j] = fmaf(s, __uint_as_float(rb[j]), acc[(c + 1) * 32 + j]);
-                    if (c + 2 < NCH)
-                        tmem_wait_ld(ra);
+                    for (int j = 0; j < 64; j += 2)
+                        fma2(acc[c * 64 + j], acc[c * 64 + j + 1], s, r[j], r[j + 1]);
                 }
                 ++kiter;
             }

@@ -149,31 +149,94 @@ __global__ void __launch_bounds__(256) rowquant_kernel(const void *__restrict__ 
     }
 }
 
+// Single-pass variant for bf16 rows with N % 1024 == 0 and N <= 32768: one
+// CTA of N/32 threads per row; thread t holds the row's 16-byte chunks t,
+// t+T, t+2T, t+3T (T = N/32, so every load and store is warp-contiguous) in
+// registers, the CTA reduces the amax through shared memory, and the row is
+// read from HBM exactly once.  Many small CTAs per SM keep the loads of
+// several rows in flight while other rows divide.
+__global__ void __launch_bounds__(1024) rowquant_bf16_cta_kernel(const uint16_t *__restrict__ x, int64_t N,
+                                                                 uint8_t *__restrict__ q, float *__restrict__ s)
+{
+    __shared__ float red[32];
+    const int T = blockDim.x;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int64_t row = blockIdx.x;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(x + row * N);
+    uint4 w[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        w[c] = __ldcs(xr + t + c * T);
+    float amax = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t u[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[j])), fabsf(bf16_hi(u[j]))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if (lane == 0)
+        red[warp] = amax;
+    __syncthreads();
+    amax = red[0];
+    for (int i = 1; i < (T >> 5); ++i)
+        amax = fmaxf(amax, red[i]);
+    const float sc = __fdiv_rn(amax, 448.0f);
+    if (t == 0)
+        s[row] = sc;
+    uint2 *qr = reinterpret_cast<uint2 *>(q + row * N);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint2 o;
+        o.x = enc4(bf16_lo(w[c].x), bf16_hi(w[c].x), bf16_lo(w[c].y), bf16_hi(w[c].y), sc);
+        o.y = enc4(bf16_lo(w[c].z), bf16_hi(w[c].z), bf16_lo(w[c].w), bf16_hi(w[c].w), sc);
+        __stcs(qr + t + c * T, o);
+    }
+}
+
 // --------------------------------------------------------------------------
 // rowdequant: y = bf16_rn(fp32(decode(q) * s[row])), 16 codes per thread.
 // --------------------------------------------------------------------------
+__device__ __forceinline__ void dequant16(const uint4 c, float sc, uint16_t *y)
+{
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float2 a = f32x2_from_e4m3x2((uint16_t)(w[j] & 0xFFFFu));
+        float2 b = f32x2_from_e4m3x2((uint16_t)(w[j] >> 16));
+        o[2 * j] = bf16x2_from_f32(__fmul_rn(a.x, sc), __fmul_rn(a.y, sc));
+        o[2 * j + 1] = bf16x2_from_f32(__fmul_rn(b.x, sc), __fmul_rn(b.y, sc));
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(y);
+    __stcs(dst, make_uint4(o[0], o[1], o[2], o[3]));
+    __stcs(dst + 1, make_uint4(o[4], o[5], o[6], o[7]));
+}
+
+// 16 codes per pack; each thread keeps 4 packs (4 x 16-byte loads) in flight.
 __global__ void __launch_bounds__(256) rowdequant_kernel(const uint8_t *__restrict__ q, const float *__restrict__ s,
                                                          int64_t M, int64_t N, uint16_t *__restrict__ y)
 {
     const int64_t n16 = M * N / 16;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
-        const int64_t e = i * 16;
-        const float sc = __ldg(s + e / N);
-        const uint4 c = __ldcs(reinterpret_cast<const uint4 *>(q + e));
-        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-        uint32_t o[8];
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+        uint4 c[4];
+        float sc[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float2 a = f32x2_from_e4m3x2((uint16_t)(w[j] & 0xFFFFu));
-            float2 b = f32x2_from_e4m3x2((uint16_t)(w[j] >> 16));
-            o[2 * j] = bf16x2_from_f32(__fmul_rn(a.x, sc), __fmul_rn(a.y, sc));
-            o[2 * j + 1] = bf16x2_from_f32(__fmul_rn(b.x, sc), __fmul_rn(b.y, sc));
+        for (int u = 0; u < 4; ++u) {
+            c[u] = __ldcs(reinterpret_cast<const uint4 *>(q + (i + u * stride) * 16));
+            sc[u] = __ldg(s + (i + u * stride) * 16 / N);
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(y + e);
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            dequant16(c[u], sc[u], y + (i + u * stride) * 16);
     }
+    for (; i < n16; i += stride)
+        dequant16(__ldcs(reinterpret_cast<const uint4 *>(q + i * 16)), __ldg(s + i * 16 / N), y + i * 16);
 }
 
 // --------------------------------------------------------------------------
@@ -380,7 +443,9 @@ cudaError_t launch_rowquant(const void *x, int x_is_bf16, int64_t M, int64_t N, 
 {
     const int64_t blocks_needed = (M + 7) / 8;
     const int grid = (int)min64(blocks_needed, (int64_t)num_sms * 8);
-    if (x_is_bf16)
+    if (x_is_bf16 && N % 1024 == 0 && N <= 32768 && M <= 0x7FFFFFFF)
+        rowquant_bf16_cta_kernel<<<(unsigned)M, (unsigned)(N / 32), 0, st>>>(static_cast<const uint16_t *>(x), N, q, s);
+    else if (x_is_bf16)
         rowquant_kernel<true><<<grid, 256, 0, st>>>(x, M, N, q, s);
     else
         rowquant_kernel<false><<<grid, 256, 0, st>>>(x, M, N, q, s);
