@@ -333,6 +333,15 @@ def run_ours(args, rank, world, local_rank):
     extra["rowdequant"] = {"us": dq_ms * 1e3, "GB/s": codec_bytes / (dq_ms * 1e-3) / 1e9,
                            "frac_of_measured_hbm": codec_bytes / (dq_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
 
+    # ---- the same layer with the slices summed inside each tile (no partials, no band reduce)
+    step_sl = lambda: g.fused_gemm_reduce(ctx, A, sa, B, sb, out, bands=P, flags=g.GEMMAR_FUSE_SLICES)
+    for _ in range(2):
+        step_sl()
+    ms_sl = time_steps(step_sl, max(5, args.steps // 2), stream)
+    extra["slice_loop_layer"] = {"us_per_layer": ms_sl * 1e3, "tflops": fl / (ms_sl * 1e-3) / 1e12,
+                                 "frac_of_fp8_peak": fl / (ms_sl * 1e-3) / 1e12 / fp8_peak,
+                                 "note": "GEMMAR_FUSE_SLICES: one fp32 chain per output over all slices"}
+
     # ---- the same layer at M = 8192
     M2 = 8192
     step_m2 = lambda: g.fused_gemm_reduce(ctx, [a[:M2] for a in A], [s[:M2] for s in sa], B, sb,
@@ -347,6 +356,11 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.empty_cache()
     Pm = 4
     Amx, eam, Bmx, ebm = make_inputs(g, ctx, Pm, M, N, K, dev, seed=7 + rank, kind=1)
+    step_mx_sl = lambda: g.fused_gemm_reduce(ctx, Amx, eam, Bmx, ebm, out, scale_kind=g.GEMMAR_SCALE_MX32, bands=Pm,
+                                             flags=g.GEMMAR_FUSE_SLICES)
+    for _ in range(2):
+        step_mx_sl()
+    ms_mx_sl = time_steps(step_mx_sl, max(5, args.steps // 2), stream)
     step_mx = lambda: g.fused_gemm_reduce(ctx, Amx, eam, Bmx, ebm, out, scale_kind=g.GEMMAR_SCALE_MX32, bands=Pm)
     for _ in range(3):
         step_mx()
@@ -359,7 +373,9 @@ def run_ours(args, rank, world, local_rank):
                       "us_per_layer": ms_mx * 1e3,
                       "gemm_us": mx_gemm_ms * 1e3,
                       "gemm_tflops": flops(Pm, M, N, K) / (mx_gemm_ms * 1e-3) / 1e12,
-                      "gemm_frac_of_fp8_peak": flops(Pm, M, N, K) / (mx_gemm_ms * 1e-3) / 1e12 / fp8_peak}
+                      "gemm_frac_of_fp8_peak": flops(Pm, M, N, K) / (mx_gemm_ms * 1e-3) / 1e12 / fp8_peak,
+                      "slice_loop_us_per_layer": ms_mx_sl * 1e3,
+                      "slice_loop_tflops": flops(Pm, M, N, K) / (ms_mx_sl * 1e-3) / 1e12}
     del Amx, eam, Bmx, ebm
     torch.cuda.empty_cache()
 

@@ -16,6 +16,14 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const TileGrid &g)
     TileCoord c;
     const int nt = t % g.ntiles_n;
     int r = t / g.ntiles_n;
+    if (g.slice_loop) {
+        c.p = 0;
+        c.b = 0;
+        c.m0 = r * 128;
+        c.n0 = nt * BN;
+        c.valid_rows = min(128, g.M - c.m0);
+        return c;
+    }
     const int mt = r % g.mt_per_band;
     r /= g.mt_per_band;
     c.p = r % g.P;
@@ -72,14 +80,46 @@ __device__ __forceinline__ void store_chunk(uint32_t stage, const uint4 (&v)[UNI
     __syncwarp();
 }
 
-// Publish one retired tile (per warp) to the band reducer: every lane's
-// stores are made visible at gpu scope, then lane 0 adds 1 with release.
+// Blocked layout of the fused path's fp32 partials (the context's own
+// workspace).  Tile i of band b, slice p (i = mt * ntiles_n + nt) owns 128*BN
+// floats at ((b * P + p) * tiles_per_band + i) * 128 * BN; inside it, the
+// 16-byte unit u (columns c*32 + 4u .. +3) of tile row q*32 + l sits at
+// float4 index ((q * BN/32 + c) * 8 + u) * 32 + l.  A warp's 32 rows of one
+// unit are therefore 512 contiguous bytes: the epilogue stores its registers
+// straight to HBM, fully coalesced and without shared-memory staging (shared
+// memory is busy feeding the tensor cores), and the band reducer transposes.
+__device__ __forceinline__ float4 *partial_tile_base(const GemmOut &o, const TileGrid &g, const TileCoord &c,
+                                                     int bn)
+{
+    const int mt = (c.m0 - c.b * g.rows_per_band) / 128;
+    const int64_t tiles_per_band = (int64_t)g.mt_per_band * g.ntiles_n;
+    const int64_t i = (int64_t)mt * g.ntiles_n + c.n0 / bn;
+    const int64_t tile = ((int64_t)c.b * g.P + c.p) * tiles_per_band + i;
+    return reinterpret_cast<float4 *>(o.out) + tile * (128 * bn / 4);
+}
+
+// Store 32 fp32 columns (chunk c) of this thread's tile row into the blocked
+// partial layout: 8 fully coalesced 512-byte warp stores.
+template <int BN>
+__device__ __forceinline__ void store_partial_chunk(float4 *tile_base, int q, int c, const float *v)
+{
+    const int lane = threadIdx.x & 31;
+    float4 *dst = tile_base + ((q * (BN / 32) + c) * 8) * 32 + lane;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+        __stcg(dst + u * 32, make_float4(v[u * 4 + 0], v[u * 4 + 1], v[u * 4 + 2], v[u * 4 + 3]));
+}
+
+// Publish one retired tile (per warp) to the band reducer: the warp barrier
+// orders every lane's stores before lane 0, whose gpu-scope fence and release
+// add then make them visible to the reducer's acquire.
 __device__ __forceinline__ void signal_band(const GemmOut &o, int band)
 {
-    __threadfence();
     __syncwarp();
-    if ((threadIdx.x & 31) == 0 && band != o.skip_band)
+    if ((threadIdx.x & 31) == 0 && band != o.skip_band) {
+        __threadfence();
         ptx::red_release_add(o.band_done + band, 1u);
+    }
 }
 
 template <int N>

@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
     const int lane = threadIdx.x & 31;
     const TileGrid &g = prm.g;
     const int KB = g.K / 128;
+    const int NKS = (g.slice_loop ? g.P : 1) * KB;   // K-blocks per tile
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -104,15 +105,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
             bool ok = true;
             for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
                 const TileCoord tc = decode_tile<BN>(t, g);
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int ks = 0; ks < NKS; ++ks) {
+                    const int p = g.slice_loop ? ks / KB : tc.p;
+                    const int kb = ks % KB;
                     if (!mbar_wait(empty + stage, ph ^ 1, abort_flag, prm.status, prm.timeout_ns,
                                    SITE_PRODUCER_EMPTY)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(full + stage, C::kStageBytes);
-                    tma_load_2d(smem + C::kOffA + stage * C::kABytes, &prm.tmA[tc.p], full + stage, kb * 128, tc.m0);
-                    tma_load_2d(smem + C::kOffB + stage * C::kBBytes, &prm.tmB[tc.p], full + stage, kb * 128, tc.n0);
+                    tma_load_2d(smem + C::kOffA + stage * C::kABytes, &prm.tmA[p], full + stage, kb * 128, tc.m0);
+                    tma_load_2d(smem + C::kOffB + stage * C::kBBytes, &prm.tmB[p], full + stage, kb * 128, tc.n0);
                     ++issued;
                     if (++stage == C::kStages) {
                         stage = 0;
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
             uint32_t ph = 0, kiter = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int ks = 0; ks < NKS; ++ks) {
                     const uint32_t buf = kiter & 1, tph = (kiter >> 1) & 1;
                     if (!mbar_wait(tempty + buf, tph ^ 1, abort_flag, prm.status, prm.timeout_ns,
                                    SITE_MMA_TMEM_EMPTY) ||
@@ -186,20 +189,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
         const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + h * HALF;
         uint32_t kiter = 0;
         bool ok = true;
+        const int nsl = g.slice_loop ? g.P : 1;
         for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
             const TileCoord tc = decode_tile<BN>(t, g);
-            const int mrow = min(tc.m0 + row, g.M - 1);
-            const float *sa_row = prm.sa[tc.p] + (int64_t)mrow * KB;
-            const float *sb_blk = prm.sb[tc.p] + (int64_t)((tc.n0 + h * HALF) >> 7) * KB;
+            const int64_t mrow = min(tc.m0 + row, g.M - 1);
+            const int64_t nblk = (tc.n0 + h * HALF) >> 7;
             float acc[HALF];
 #pragma unroll
             for (int j = 0; j < HALF; ++j)
                 acc[j] = 0.0f;
+            // scales of the tile's K-steps, slice by slice: sa[p][row, kb] * sb[p][n/128, kb],
+            // each loaded one step ahead
+            const float *sa_row = prm.sa[tc.p] + mrow * KB;
+            const float *sb_blk = prm.sb[tc.p] + nblk * KB;
             float s_next = __ldg(sa_row) * __ldg(sb_blk);
-            for (int kb = 0; kb < KB; ++kb) {
+            for (int ks = 0, sl = 0, kb = 0; ks < NKS; ++ks) {
                 const float s = s_next;
-                if (kb + 1 < KB)
-                    s_next = __ldg(sa_row + kb + 1) * __ldg(sb_blk + kb + 1);
+                if (++kb == KB) {
+                    kb = 0;
+                    if (++sl < nsl) {
+                        sa_row = prm.sa[sl] + mrow * KB;
+                        sb_blk = prm.sb[sl] + nblk * KB;
+                    }
+                }
+                if (ks + 1 < NKS)
+                    s_next = __ldg(sa_row + kb) * __ldg(sb_blk + kb);
                 const uint32_t buf = kiter & 1, tph = (kiter >> 1) & 1;
                 if (!mbar_wait(tfull + buf, tph, abort_flag, prm.status, prm.timeout_ns, SITE_EPI_TMEM_FULL)) {
                     ok = false;
@@ -243,6 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
                     }
                     store_chunk<4>(staging, v, base + c * 64, (int64_t)g.N * 2, rows_valid);
                 }
+            } else if (prm.o.out_mode == OUT_PARTIAL_F32) {
+                float4 *tb = partial_tile_base(prm.o, g, tc, BN);
+#pragma unroll
+                for (int c = 0; c < NCH; ++c)
+                    store_partial_chunk<BN>(tb, q, h * NCH + c, &acc[c * 32]);
             } else {
                 char *base = tile_out_base(prm.o, g, tc, 4) + ((int64_t)q * 32 * g.N + h * HALF) * 4;
 #pragma unroll
@@ -256,9 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
                     }
                     store_chunk<8>(staging, v, base + c * 128, (int64_t)g.N * 4, rows_valid);
                 }
-                if (prm.o.out_mode == OUT_PARTIAL_F32)
-                    signal_band(prm.o, tc.b);
             }
+            if (prm.o.out_mode == OUT_PARTIAL_F32)
+                signal_band(prm.o, tc.b);
         }
     }
 

@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
     const int lane = threadIdx.x & 31;
     const TileGrid &g = prm.g;
     const int KB = g.K / 128;
+    const int NKS = (g.slice_loop ? g.P : 1) * KB;   // K-blocks per tile
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -108,9 +109,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
             for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
                 const TileCoord tc = decode_tile<BN>(t, g);
                 const int mt = (tc.m0 - tc.b * g.rows_per_band) / 128;
-                const int64_t a_img = ((int64_t)(tc.p * g.bands + tc.b) * g.mt_per_band + mt) * KB;
-                const int64_t b_img = ((int64_t)tc.p * g.ntiles_n + tc.n0 / BN) * KB;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int ks = 0; ks < NKS; ++ks) {
+                    const int p = g.slice_loop ? ks / KB : tc.p;
+                    const int kb = ks % KB;
+                    const int64_t a_img = ((int64_t)(p * g.bands + tc.b) * g.mt_per_band + mt) * KB;
+                    const int64_t b_img = ((int64_t)p * g.ntiles_n + tc.n0 / BN) * KB;
                     if (!mbar_wait(empty + stage, ph ^ 1, abort_flag, prm.status, prm.timeout_ns,
                                    SITE_PRODUCER_EMPTY)) {
                         ok = false;
@@ -118,8 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                     }
                     uint8_t *sf = smem + C::kOffSf + stage * C::kSfBytes;
                     mbar_arrive_expect_tx(full + stage, C::kStageBytes);
-                    tma_load_2d(smem + C::kOffA + stage * C::kABytes, &prm.tmA[tc.p], full + stage, kb * 128, tc.m0);
-                    tma_load_2d(smem + C::kOffB + stage * C::kBBytes, &prm.tmB[tc.p], full + stage, kb * 128, tc.n0);
+                    tma_load_2d(smem + C::kOffA + stage * C::kABytes, &prm.tmA[p], full + stage, kb * 128, tc.m0);
+                    tma_load_2d(smem + C::kOffB + stage * C::kBBytes, &prm.tmB[p], full + stage, kb * 128, tc.n0);
                     bulk_load(sf, prm.sfa + (a_img + kb) * 512, 512, full + stage);
                     bulk_load(sf + 512, prm.sfb + (b_img + kb) * 1024, 1024, full + stage);
                     ++issued;
@@ -153,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                                SITE_MMA_TMEM_EMPTY))
                     break;
                 const uint32_t d = tmem_base + buf * BN;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int ks = 0; ks < NKS; ++ks) {
                     if (!mbar_wait(full + stage, ph, abort_flag, prm.status, prm.timeout_ns, SITE_MMA_FULL)) {
                         ok = false;
                         break;
@@ -168,9 +171,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         mma_mxf8(d, ad + 2 * k, bd + 2 * k, idesc_mx_e4m3(128, BN, (uint32_t)k), sfa_t, sfb_t,
-                                 (kb > 0 || k > 0) ? 1u : 0u);
+                                 (ks > 0 || k > 0) ? 1u : 0u);
                     tc_commit(empty + stage);
-                    if (kb == KB - 1)
+                    if (ks == NKS - 1)
                         tc_commit(tfull + buf);
                     if (++stage == C::kStages) {
                         stage = 0;
@@ -225,6 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                                           bf16x2_from_f32(__uint_as_float(r[u * 8 + 4]), __uint_as_float(r[u * 8 + 5])),
                                           bf16x2_from_f32(__uint_as_float(r[u * 8 + 6]), __uint_as_float(r[u * 8 + 7])));
                     store_chunk<4>(staging, v, base + c * 64, (int64_t)g.N * 2, rows_valid);
+                } else if (prm.o.out_mode == OUT_PARTIAL_F32) {
+                    store_partial_chunk<BN>(partial_tile_base(prm.o, g, tc, BN), q, c,
+                                            reinterpret_cast<const float *>(r));
                 } else {
                     uint4 v[8];
 #pragma unroll

@@ -136,9 +136,11 @@ int shape_rules(int P, int64_t M, int64_t N, int64_t K, int bands, int scale_kin
 int bs_tile_n(int64_t N) { return (N % 256 == 0) ? 256 : 128; }
 int mx_tile_n(int64_t N) { return (N % 224 == 0) ? 224 : 128; }
 
-TileGrid make_grid(int P, int64_t M, int64_t N, int64_t K, int bands, int bn)
+TileGrid make_grid(int P, int64_t M, int64_t N, int64_t K, int bands, int bn, int slice_loop = 0)
 {
     TileGrid g;
+    if (slice_loop)
+        bands = 1;
     g.P = P;
     g.M = (int)M;
     g.N = (int)N;
@@ -147,7 +149,8 @@ TileGrid make_grid(int P, int64_t M, int64_t N, int64_t K, int bands, int bn)
     g.rows_per_band = (int)(M / bands);
     g.mt_per_band = (g.rows_per_band + 127) / 128;
     g.ntiles_n = (int)(N / bn);
-    g.num_tiles = bands * P * g.mt_per_band * g.ntiles_n;
+    g.slice_loop = slice_loop;
+    g.num_tiles = (slice_loop ? 1 : P) * bands * g.mt_per_band * g.ntiles_n;
     return g;
 }
 
@@ -177,7 +180,7 @@ int64_t mx_sfb_bytes(int P, int64_t N, int64_t K, int bn) { return (int64_t)P * 
 // the result goes.
 int run_gemm(gemmar_ctx *ctx, int P, const uint8_t *const *A, const void *const *sa, const uint8_t *const *B,
              const void *const *sb, int scale_kind, int64_t M, int64_t N, int64_t K, int bands, const GemmOut &o,
-             cudaStream_t st)
+             cudaStream_t st, int slice_loop = 0)
 {
     if (!load_encode())
         return GEMMAR_ERR_CUDA;
@@ -193,7 +196,7 @@ int run_gemm(gemmar_ctx *ctx, int P, const uint8_t *const *A, const void *const 
             prm.sa[p] = static_cast<const float *>(sa[p]);
             prm.sb[p] = static_cast<const float *>(sb[p]);
         }
-        prm.g = make_grid(P, M, N, K, bands, bn);
+        prm.g = make_grid(P, M, N, K, bands, bn, slice_loop);
         prm.o = o;
         prm.status = ctx->status;
         prm.timeout_ns = ctx->timeout_ns;
@@ -201,6 +204,8 @@ int run_gemm(gemmar_ctx *ctx, int P, const uint8_t *const *A, const void *const 
         CUDA_OK(launch_gemm_blockscale(prm, bn, grid, st));
     } else {
         const int bn = mx_tile_n(N);
+        if (slice_loop)
+            bands = 1;
         if (mx_sfa_bytes(P, M, K, bands) > ctx->sfa_bytes || mx_sfb_bytes(P, N, K, bn) > ctx->sfb_bytes)
             return GEMMAR_ERR_WORKSPACE;
         CUDA_OK(launch_mx_repack(reinterpret_cast<const uint8_t *const *>(sa),
@@ -213,7 +218,7 @@ int run_gemm(gemmar_ctx *ctx, int P, const uint8_t *const *A, const void *const 
                 return GEMMAR_ERR_CUDA;
         prm.sfa = ctx->sfa;
         prm.sfb = ctx->sfb;
-        prm.g = make_grid(P, M, N, K, bands, bn);
+        prm.g = make_grid(P, M, N, K, bands, bn, slice_loop);
         prm.o = o;
         prm.status = ctx->status;
         prm.timeout_ns = ctx->timeout_ns;
@@ -407,27 +412,39 @@ GEMMAR_API int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A
     }
     if (!aligned16(out))
         return GEMMAR_ERR_ALIGN;
-    if ((int64_t)P * M * N > ctx->W_floats)
+    const bool slices = (flags & GEMMAR_FUSE_SLICES) != 0;
+    if (!slices && blocked_partial_floats(P, M, bands, N) > ctx->W_floats)
         return GEMMAR_ERR_WORKSPACE;
     if ((flags & GEMMAR_FP8_WIRE) && M * N > ctx->max_M * ctx->N)
         return GEMMAR_ERR_WORKSPACE;
     cudaStream_t st = as_stream(stream);
-    CUDA_OK(cudaMemsetAsync(ctx->band_done, 0, sizeof(uint32_t) * bands, st));
-    if (flags & GEMMAR_DEBUG_CANARY) {
-        CUDA_OK(cudaMemsetAsync(ctx->W, 0xFF, sizeof(float) * (size_t)(P * M * N), st));
-        CUDA_OK(cudaMemsetAsync(out, 0xFF, sizeof(uint16_t) * (size_t)(M * N), st));
+    if (slices) {
+        // every tile accumulates all P slices itself: no partials, no band reduce
+        if (flags & GEMMAR_DEBUG_CANARY)
+            CUDA_OK(cudaMemsetAsync(out, 0xFF, sizeof(uint16_t) * (size_t)(M * N), st));
+        mark(ctx, GEMMAR_PHASE_GEMM, st);
+        GemmOut os{out, nullptr, OUT_BF16, -1};
+        if ((rc = run_gemm(ctx, P, A, sa, B, sb, scale_kind, M, N, K, 1, os, st, 1)))
+            return rc;
+        mark(ctx, GEMMAR_PHASE_REDUCE, st);
+    } else {
+        CUDA_OK(cudaMemsetAsync(ctx->band_done, 0, sizeof(uint32_t) * bands, st));
+        if (flags & GEMMAR_DEBUG_CANARY) {
+            CUDA_OK(cudaMemsetAsync(ctx->W, 0xFF, sizeof(float) * (size_t)blocked_partial_floats(P, M, bands, N), st));
+            CUDA_OK(cudaMemsetAsync(out, 0xFF, sizeof(uint16_t) * (size_t)(M * N), st));
+        }
+        GemmOut o{ctx->W, ctx->band_done, OUT_PARTIAL_F32, (flags & GEMMAR_FAULT_SKIP_BAND) ? 0 : -1};
+        mark(ctx, GEMMAR_PHASE_GEMM, st);
+        if ((rc = run_gemm(ctx, P, A, sa, B, sb, scale_kind, M, N, K, bands, o, st)))
+            return rc;
+        mark(ctx, GEMMAR_PHASE_REDUCE, st);
+        const int bn = scale_kind == GEMMAR_SCALE_BLOCK128 ? bs_tile_n(N) : mx_tile_n(N);
+        const TileGrid g = make_grid(P, M, N, K, bands, bn);
+        // every epilogue warp (8 per tile) signals once per retired tile
+        const uint32_t expected = (uint32_t)(g.mt_per_band * g.ntiles_n * P * 8);
+        CUDA_OK(launch_band_reduce_blocked(ctx->W, out, P, M, N, bands, bn, ctx->band_done, expected, ctx->status,
+                                           ctx->timeout_ns, ctx->num_sms * 8, st));
     }
-    GemmOut o{ctx->W, ctx->band_done, OUT_PARTIAL_F32, (flags & GEMMAR_FAULT_SKIP_BAND) ? 0 : -1};
-    mark(ctx, GEMMAR_PHASE_GEMM, st);
-    if ((rc = run_gemm(ctx, P, A, sa, B, sb, scale_kind, M, N, K, bands, o, st)))
-        return rc;
-    mark(ctx, GEMMAR_PHASE_REDUCE, st);
-    const int bn = scale_kind == GEMMAR_SCALE_BLOCK128 ? bs_tile_n(N) : mx_tile_n(N);
-    const TileGrid g = make_grid(P, M, N, K, bands, bn);
-    // every epilogue warp (8 per tile) signals once per retired tile
-    const uint32_t expected = (uint32_t)(g.mt_per_band * g.ntiles_n * P * 8);
-    CUDA_OK(launch_band_reduce(ctx->W, out, P, M, N, bands, ctx->band_done, expected, ctx->status, ctx->timeout_ns,
-                               ctx->num_sms * 8, st));
     mark(ctx, GEMMAR_PHASE_QUANTIZE, st);
     if (flags & GEMMAR_FP8_WIRE)
         CUDA_OK(launch_rowquant(out, 1, M, N, ctx->wire_q, ctx->wire_s, ctx->num_sms, st));
@@ -574,7 +591,9 @@ GEMMAR_API int gemmar_create(gemmar_ctx **out, int device, int64_t max_M, int64_
     ctx->max_P = max_P;
     ctx->flags = flags;
     ctx->timeout_ns = wait_timeout_ns > 0 ? (uint64_t)wait_timeout_ns : 2000000000ull;
-    ctx->W_floats = (int64_t)max_P * max_M * N;
+    // fp32 partials in the tile-blocked layout: every band padded to whole
+    // 128-row tiles, for up to max_P bands
+    ctx->W_floats = (int64_t)max_P * (max_M + 128 * max_P) * N;
     // mx repack images, sized for the largest tile count any band split can give
     ctx->sfa_bytes = (int64_t)max_P * ((max_M + 127) / 128 + kMaxBands) * (K / 128) * 512;
     ctx->sfb_bytes = (int64_t)max_P * (N / 128) * (K / 128) * 1024;

@@ -22,10 +22,13 @@ enum OutMode : int {
 // Work decomposition shared by both GEMM kernels: tile t covers rows
 // [m0, m0 + min(128, band end - m0)) and columns [n0, n0 + BN) of slice p in
 // band b, with t = ((b * P + p) * mt_per_band + mt) * ntiles_n + nt, i.e. in
-// band order so that band 0's partials are complete first.
+// band order so that band 0's partials are complete first.  With slice_loop
+// a tile instead runs over every slice (K-steps p*K/128 + kb) and its one
+// accumulator holds the P-way sum.
 struct TileGrid {
     int P, M, N, K;
     int bands, rows_per_band, mt_per_band, ntiles_n, num_tiles;
+    int slice_loop;   // 1: a tile covers all P slices (bands == 1, t = mt * ntiles_n + nt)
 };
 
 struct GemmOut {
@@ -74,6 +77,16 @@ cudaError_t launch_mx_repack(const uint8_t *const *ea, const uint8_t *const *eb,
 cudaError_t launch_band_reduce(const float *W, uint16_t *out, int P, int64_t M, int64_t N, int bands,
                                const uint32_t *band_done, uint32_t expected, ptx::DevStatus *status,
                                uint64_t timeout_ns, int grid_blocks, cudaStream_t s);
+// The same reduce over the fused path's tile-blocked partials (layout: epilogue.cuh).
+cudaError_t launch_band_reduce_blocked(const float *W, uint16_t *out, int P, int64_t M, int64_t N, int bands,
+                                       int bn, const uint32_t *band_done, uint32_t expected, ptx::DevStatus *status,
+                                       uint64_t timeout_ns, int grid_blocks, cudaStream_t s);
+// Floats of blocked partials a fused call needs (ragged bands pad tiles to 128 rows).
+inline int64_t blocked_partial_floats(int P, int64_t M, int bands, int64_t N)
+{
+    const int64_t rpb = M / bands, mtpb = (rpb + 127) / 128;
+    return (int64_t)P * bands * mtpb * 128 * N;
+}
 cudaError_t launch_rowquant(const void *x, int x_is_bf16, int64_t M, int64_t N, uint8_t *q, float *s,
                             int num_sms, cudaStream_t st);
 cudaError_t launch_rowdequant(const uint8_t *q, const float *s, int64_t M, int64_t N, uint16_t *y, int num_sms,

@@ -111,7 +111,7 @@ extern "C" __attribute__((visibility("default"))) int fused_gemm_reduce_noalloc(
     if (bands > 1024 || bands > M || M % bands != 0 || N % 128 != 0 || K % 128 != 0 || N > 65536 || K > 65536 ||
         M > (int64_t(1) << 24))
         return GEMMAR_ERR_SHAPE;
-    if ((int64_t)P * M * N > GEMMAR_NOALLOC_MAX_PARTIALS)
+    if (blocked_partial_floats(P, M, bands, N) > GEMMAR_NOALLOC_MAX_PARTIALS)
         return GEMMAR_ERR_WORKSPACE;   // beyond the fixed scratch: use fused_gemm_reduce
     for (int p = 0; p < P; ++p) {
         if (!A[p] || !sa[p] || !B[p] || !sb[p])
@@ -163,8 +163,8 @@ extern "C" __attribute__((visibility("default"))) int fused_gemm_reduce_noalloc(
     if (launch_gemm_blockscale(prm, bn, g.num_tiles < s->num_sms ? g.num_tiles : s->num_sms, st) != cudaSuccess)
         return GEMMAR_ERR_CUDA;
     const uint32_t expected = (uint32_t)(g.mt_per_band * g.ntiles_n * P * 8);
-    if (launch_band_reduce(s->partials, out, P, M, N, bands, s->band_done, expected, s->status, kTimeoutNs,
-                           s->num_sms * 8, st) != cudaSuccess)
+    if (launch_band_reduce_blocked(s->partials, out, P, M, N, bands, bn, s->band_done, expected, s->status,
+                                   kTimeoutNs, s->num_sms * 8, st) != cudaSuccess)
         return GEMMAR_ERR_CUDA;
     return GEMMAR_OK;
 }

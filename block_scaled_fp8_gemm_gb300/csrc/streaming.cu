@@ -86,6 +86,98 @@ __global__ void __launch_bounds__(256) band_reduce_kernel(const float *__restric
 }
 
 // --------------------------------------------------------------------------
+// band_reduce over the fused path's blocked partials (layout: epilogue.cuh).
+// One warp reduces one 32-row x 32-column block of a tile: for each of its
+// 8 column units it loads the unit from every slice (512 contiguous bytes per
+// slice and warp), sums in fp32 with p ascending, rounds to bf16 and parks
+// the row's 64 bytes in registers; a warp-private shared transpose then
+// writes 8 rows x 64 bytes per store instruction.  Rows past the band end
+// (ragged bands) are not written.  Same arithmetic as band_reduce_kernel.
+// --------------------------------------------------------------------------
+template <int P>
+__global__ void __launch_bounds__(256) band_reduce_blocked_kernel(const float4 *__restrict__ W,
+                                                                  uint16_t *__restrict__ out, int M, int N,
+                                                                  int bands, int rows_per_band, int mt_per_band,
+                                                                  int ntiles_n, int bn, const uint32_t *band_done,
+                                                                  uint32_t expected, DevStatus *status,
+                                                                  uint64_t timeout_ns)
+{
+    __shared__ int band_ok;
+    __shared__ __align__(16) uint32_t stage[8][32 * 16];   // per warp: 32 rows x 64 bytes
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nchunk = bn / 32;
+    const int64_t tiles_per_band = (int64_t)mt_per_band * ntiles_n;
+    const int64_t blocks_per_band = tiles_per_band * 4 * nchunk;   // (tile, q, c) blocks
+    const int64_t tile_f4 = 128 * bn / 4;
+    const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+    uint32_t *st = stage[warp];
+    for (int b = 0; b < bands; ++b) {
+        if (band_done != nullptr) {
+            if (threadIdx.x == 0) {
+                int ok = 1;
+                if (ld_acquire(band_done + b) < expected) {
+                    const uint64_t t0 = globaltimer();
+                    while (ld_acquire(band_done + b) < expected) {
+                        if (*(volatile int *)&status->code != 0) { ok = 0; break; }
+                        if (globaltimer() - t0 > timeout_ns) {
+                            report(status, kErrTimeout, SITE_REDUCE_BAND);
+                            ok = 0;
+                            break;
+                        }
+                        __nanosleep(256);
+                    }
+                }
+                band_ok = ok;
+            }
+            __syncthreads();
+            if (!band_ok)
+                return;
+        }
+        for (int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp; blk < blocks_per_band; blk += warps_total) {
+            const int c = (int)(blk % nchunk);
+            const int q = (int)((blk / nchunk) % 4);
+            const int64_t i = blk / (4 * nchunk);
+            const int mt = (int)(i / ntiles_n), nt = (int)(i % ntiles_n);
+            // float4 index of (band b, slice 0, tile i, q, c, unit 0, lane)
+            const float4 *src = W + ((int64_t)b * P * tiles_per_band + i) * tile_f4 + ((q * nchunk + c) * 8) * 32 + lane;
+            uint32_t o[16];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                float4 v[P];
+#pragma unroll
+                for (int p = 0; p < P; ++p)
+                    v[p] = __ldcs(src + (int64_t)p * tiles_per_band * tile_f4 + u * 32);
+                float4 a = v[0];
+#pragma unroll
+                for (int p = 1; p < P; ++p) {
+                    a.x = a.x + v[p].x; a.y = a.y + v[p].y; a.z = a.z + v[p].z; a.w = a.w + v[p].w;
+                }
+                o[2 * u] = bf16x2_from_f32(a.x, a.y);
+                o[2 * u + 1] = bf16x2_from_f32(a.z, a.w);
+            }
+            // transpose: row `lane` holds 64 bytes (16 words), XOR-swizzled by 16-byte unit
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4 *>(st + lane * 16 + ((j ^ ((lane >> 1) & 3)) * 4)) =
+                    make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+            __syncwarp();
+            const int row0 = mt * 128 + q * 32;                      // tile row within the band
+            const int64_t col = (int64_t)nt * bn + c * 32;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int r = k * 8 + (lane >> 2), j = lane & 3;
+                const uint4 val = *reinterpret_cast<const uint4 *>(st + r * 16 + ((j ^ ((r >> 1) & 3)) * 4));
+                if (row0 + r < rows_per_band) {
+                    const int64_t m = (int64_t)b * rows_per_band + row0 + r;
+                    *reinterpret_cast<uint4 *>(out + m * N + col + j * 8) = val;
+                }
+            }
+            __syncwarp();
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
 // rowquant: one warp per row.  Pass 1 streams the row for its amax (warp
 // shuffle max); pass 2 re-reads it (L1/L2 hit) and writes the codes.
 // s = fp32(amax / 448) and codes = e4m3_rn_sat(fp32(x / s)), IEEE divisions.
@@ -149,13 +241,13 @@ __global__ void __launch_bounds__(256) rowquant_kernel(const void *__restrict__ 
     }
 }
 
-// Single-pass variant for bf16 rows with N % 1024 == 0 and N <= 32768: one
+// Single-pass variant for bf16 rows with N % 1024 == 0 and N <= 8192: one
 // CTA of N/32 threads per row; thread t holds the row's 16-byte chunks t,
 // t+T, t+2T, t+3T (T = N/32, so every load and store is warp-contiguous) in
 // registers, the CTA reduces the amax through shared memory, and the row is
 // read from HBM exactly once.  Many small CTAs per SM keep the loads of
 // several rows in flight while other rows divide.
-__global__ void __launch_bounds__(1024) rowquant_bf16_cta_kernel(const uint16_t *__restrict__ x, int64_t N,
+__global__ void __launch_bounds__(256, 5) rowquant_bf16_cta_kernel(const uint16_t *__restrict__ x, int64_t N,
                                                                  uint8_t *__restrict__ q, float *__restrict__ s)
 {
     __shared__ float red[32];
@@ -438,12 +530,33 @@ cudaError_t launch_band_reduce(const float *W, uint16_t *out, int P, int64_t M, 
     return cudaGetLastError();
 }
 
+cudaError_t launch_band_reduce_blocked(const float *W, uint16_t *out, int P, int64_t M, int64_t N, int bands,
+                                       int bn, const uint32_t *band_done, uint32_t expected, DevStatus *status,
+                                       uint64_t timeout_ns, int grid_blocks, cudaStream_t s)
+{
+    const int rpb = (int)(M / bands), mtpb = (rpb + 127) / 128, ntn = (int)(N / bn);
+    const float4 *w4 = reinterpret_cast<const float4 *>(W);
+    dim3 grid(grid_blocks), block(256);
+#define GEMMAR_REDUCE_BLK_CASE(PP)                                                                                \
+    case PP:                                                                                                      \
+        band_reduce_blocked_kernel<PP><<<grid, block, 0, s>>>(w4, out, (int)M, (int)N, bands, rpb, mtpb, ntn, bn, \
+                                                              band_done, expected, status, timeout_ns);           \
+        break;
+    switch (P) {
+        GEMMAR_REDUCE_BLK_CASE(1) GEMMAR_REDUCE_BLK_CASE(2) GEMMAR_REDUCE_BLK_CASE(3) GEMMAR_REDUCE_BLK_CASE(4)
+        GEMMAR_REDUCE_BLK_CASE(5) GEMMAR_REDUCE_BLK_CASE(6) GEMMAR_REDUCE_BLK_CASE(7) GEMMAR_REDUCE_BLK_CASE(8)
+        default: return cudaErrorInvalidValue;
+    }
+#undef GEMMAR_REDUCE_BLK_CASE
+    return cudaGetLastError();
+}
+
 cudaError_t launch_rowquant(const void *x, int x_is_bf16, int64_t M, int64_t N, uint8_t *q, float *s, int num_sms,
                             cudaStream_t st)
 {
     const int64_t blocks_needed = (M + 7) / 8;
     const int grid = (int)min64(blocks_needed, (int64_t)num_sms * 8);
-    if (x_is_bf16 && N % 1024 == 0 && N <= 32768 && M <= 0x7FFFFFFF)
+    if (x_is_bf16 && N % 1024 == 0 && N <= 8192 && M <= 0x7FFFFFFF)
         rowquant_bf16_cta_kernel<<<(unsigned)M, (unsigned)(N / 32), 0, st>>>(static_cast<const uint16_t *>(x), N, q, s);
     else if (x_is_bf16)
         rowquant_kernel<true><<<grid, 256, 0, st>>>(x, M, N, q, s);

@@ -80,6 +80,8 @@ enum { GEMMAR_SCALE_BLOCK128 = 0, GEMMAR_SCALE_MX32 = 1 };
 #define GEMMAR_FAULT_SKIP_BAND (1u << 2)  /* fused, testing only: band 0 is never signalled, so the
                                              reducer's bounded wait expires (GEMMAR_ERR_TIMEOUT) */
 #define GEMMAR_NO_SELF_TEST    (1u << 3)  /* create: skip the closed-form self-test */
+#define GEMMAR_FUSE_SLICES     (1u << 4)  /* fused: each output tile accumulates all P slices itself (no
+                                             partials, no band reduce); see fused_gemm_reduce */
 
 /* Largest number of K-slices ("ranks") one call takes. */
 #define GEMMAR_MAX_P 8
@@ -99,7 +101,9 @@ int gemmar_supports(int P, int64_t M, int64_t N, int64_t K, int bands, int scale
 /*
  * gemmar_create -- make a context on `device` (which must be current) whose
  * workspace serves fused_gemm_reduce calls with P <= max_P, M <= max_M and the
- * given N and K: fp32 partials of max_P*max_M*N floats, band counters, the
+ * given N and K: fp32 partials of max_P*(max_M + 128*max_P)*N floats (a tile-
+ * blocked layout; each band's rows are rounded up to whole 128-row tiles),
+ * band counters, the
  * mxfp8 scale repack area and the fp8-wire staging.  Like the pages' window
  * it is sized once and never grows (sglang pull request #40757, "Worth a
  * reviewer's attention": the window is sized from the chunked-prefill
@@ -240,6 +244,15 @@ int quant_mx_e4m3(gemmar_ctx *ctx, const float *x, int64_t R, int64_t C, uint8_t
  *   (GEMMAR_SCALE_MX32).  bands: row bands (0 = P).  out: bf16 [M,N].
  * Deterministic: equal, bit for bit, to P x gemm_*(F32) into W followed by
  * band_reduce, and to itself on a rerun.
+ *
+ * With GEMMAR_FUSE_SLICES the slices are instead summed inside each output
+ * tile: one fp32 accumulation chain per output element over (p, K-block) in
+ * the fixed order p = 0..P-1, K ascending, rounded once to bf16.  Nothing is
+ * stored between the slices, so the partial write and the band reduce
+ * (2 x P*M*N*4 bytes) disappear; the result is deterministic and within the
+ * same tolerance of the definition, but its fp32 rounding order differs from
+ * the band path's, so the two are not bit-equal.  bands is then ignored
+ * (it must still satisfy the shape rules).
  */
 int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A, const void *const *sa,
                       const uint8_t *const *B, const void *const *sb, int scale_kind,
@@ -258,15 +271,16 @@ int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A, const voi
  * own allocator.  Neither can call gemmar_create, which allocates.  This call
  * takes no context and allocates nothing (no cudaMalloc, no cudaFree, no
  * allocating library routine): its scratch -- fp32 partials for up to
- * GEMMAR_NOALLOC_MAX_PARTIALS elements (P*M*N), 1024 band counters and a
- * status word -- lives in fixed-size arrays in the library's device code,
+ * GEMMAR_NOALLOC_MAX_PARTIALS elements (P*M*N, each band's rows rounded up to
+ * whole 128-row tiles), 1024 band counters and a status word -- lives in fixed-size arrays in the library's device code,
  * which the CUDA driver reserves on every GPU that loads the library (32 MiB
  * plus a few KiB per GPU) and keeps until the process exits.
  *
  * Arguments as fused_gemm_reduce with scale_kind GEMMAR_SCALE_BLOCK128 and no
  * flags: A, sa, B, sb are HOST arrays of P device pointers, out is bf16 [M,N]
  * on the current device, bands 0 means P.  Returns GEMMAR_ERR_WORKSPACE when
- * P*M*N exceeds GEMMAR_NOALLOC_MAX_PARTIALS (use fused_gemm_reduce then), and
+ * that padded P*M*N exceeds GEMMAR_NOALLOC_MAX_PARTIALS (use fused_gemm_reduce
+ * then), and
  * the other codes as fused_gemm_reduce.  The result equals fused_gemm_reduce's
  * bit for bit (same kernels, same fixed-order reduce).
  *

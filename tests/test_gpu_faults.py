@@ -39,9 +39,9 @@ def test_host_side_errors_launch_nothing(g):
     with pytest.raises(g.GemmarError) as e:     # M not a multiple of the band count
         g.fused_gemm_reduce(ctx, dA, dsa, dB, dsb, out, bands=3)
     assert e.value.code == g.GEMMAR_ERR_SHAPE
-    big = [torch.zeros((512, 256), dtype=torch.uint8, device="cuda")] * 2
-    bigs = [torch.ones((512, 2), dtype=torch.float32, device="cuda")] * 2
-    out2 = torch.empty((512, 512), dtype=torch.bfloat16, device="cuda")
+    big = [torch.zeros((1024, 256), dtype=torch.uint8, device="cuda")] * 2
+    bigs = [torch.ones((1024, 2), dtype=torch.float32, device="cuda")] * 2
+    out2 = torch.empty((1024, 512), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(g.GemmarError) as e:     # more rows than the workspace was sized for
         g.fused_gemm_reduce(ctx, big, bigs, dB, dsb, out2)
     assert e.value.code == g.GEMMAR_ERR_WORKSPACE

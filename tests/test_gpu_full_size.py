@@ -1,0 +1,129 @@
+"""Parity at the full workload sizes, in the launch configuration the
+benchmark times (fused_gemm_reduce, bands = P), on sampled output rows the
+oracle computes one by one: the first, second, middle and last rows of every
+band plus random rows, all columns.
+
+  - wo_b prefill: P=8, A_p [4096, 2048], B_p [7168, 2048], blockscale
+  - wo_b full chunk: the same at M = 8192 and M = 16384 (the headline shape)
+  - fp8 wire on the M = 16384 output
+  - mxfp8: P=4, A_p [16384, 2048], B_p [7168, 2048], ue8m0 1x32
+
+Operands are drawn by `synthetic` and quantised by the oracle on the host, so
+both sides consume identical codes and scales.  The M=4096 and M=8192 cases
+use the leading rows of the M=16384 operands (same generator streams).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import blockscale_operands, check_bf16_output, mx_operands, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+P, MMAX, N, K = 8, 16384, 7168, 2048
+
+
+def sample_rows(M, bands, per_band_random=2, seed=0):
+    rng = np.random.default_rng(seed)
+    rpb = M // bands
+    rows = []
+    for b in range(bands):
+        base = b * rpb
+        rows += [base, base + 1, base + rpb // 2, base + rpb - 1]
+        rows += list(base + rng.integers(0, rpb, per_band_random))
+    return np.unique(np.array(rows, dtype=np.int64))
+
+
+@pytest.fixture(scope="module")
+def g():
+    import block_scaled_fp8_gemm_gb300 as g
+    return g
+
+
+@pytest.fixture(scope="module")
+def headline(g):
+    A, sa, B, sb = blockscale_operands(P, MMAX, N, K, seed=0)
+    torch.cuda.set_device(0)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    d = dict(A=A, sa=sa, B=B, sb=sb, dA=[dev(a) for a in A], dsa=[dev(s) for s in sa],
+             dB=[dev(b) for b in B], dsb=[dev(s) for s in sb])
+    ctx = g.gemmar_create(0, MMAX, N, K, P)
+    d["ctx"] = ctx
+    yield d
+    ctx.close()
+
+
+def run_fused(g, d, M, flags=0):
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    g.fused_gemm_reduce(d["ctx"], [a[:M] for a in d["dA"]], [s[:M] for s in d["dsa"]], d["dB"], d["dsb"],
+                        out, bands=P, flags=flags)
+    torch.cuda.synchronize()
+    code, detail = g.gemmar_status(d["ctx"])
+    assert code == 0, (code, detail)
+    return out
+
+
+def oracle_rows(d, M, rows):
+    return oracle.gemm_reduce([a[:M] for a in d["A"]], [s[:M] for s in d["sa"]], d["B"], d["sb"], 0, rows=rows)
+
+
+@pytest.mark.parametrize("M", [4096, 8192, 16384])
+def test_fused_blockscale_full_size(g, headline, M):
+    rows = sample_rows(M, P, seed=M)
+    out = run_fused(g, headline, M)
+    got = out[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    ref, _ = oracle_rows(headline, M, rows)
+    rl = check_bf16_output(got, ref, f"fused P=8 M={M} N={N} K={K}")
+    assert rl < 2.35e-3      # below the pages' bf16-partial level, as fp32 partials should be
+    # every output written, nothing non-finite anywhere
+    assert torch.isfinite(out.float()).all()
+
+
+def test_fused_slice_loop_full_size(g, headline):
+    M = MMAX
+    rows = sample_rows(M, P, seed=7)
+    out = run_fused(g, headline, M, flags=g.GEMMAR_FUSE_SLICES)
+    got = out[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    ref, _ = oracle_rows(headline, M, rows)
+    check_bf16_output(got, ref, f"fused slice loop P=8 M={M}")
+    assert torch.isfinite(out.float()).all()
+
+
+def test_fused_full_size_is_deterministic(g, headline):
+    a = run_fused(g, headline, MMAX)
+    b = run_fused(g, headline, MMAX, flags=g.GEMMAR_DEBUG_CANARY)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_fp8_wire_full_size(g, headline):
+    M = MMAX
+    rows = sample_rows(M, P, seed=3)
+    wire = run_fused(g, headline, M, flags=g.GEMMAR_FP8_WIRE)
+    got = wire[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    ref, ref16 = oracle_rows(headline, M, rows)
+    q, s = oracle.rowquant(oracle.bf16_to_f32(ref16))
+    wire_ref = oracle.bf16_to_f32(oracle.rowdequant(q, s))
+    assert rel_l2(got, ref) <= 3e-2
+    assert rel_l2(got, wire_ref) <= 1e-2
+
+
+def test_fused_mx_full_size(g):
+    Pm, M = 4, MMAX
+    A, ea, B, eb = mx_operands(Pm, M, N, K, seed=4)
+    torch.cuda.set_device(0)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    ctx = g.gemmar_create(0, M, N, K, Pm)
+    try:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        g.fused_gemm_reduce(ctx, [dev(a) for a in A], [dev(s) for s in ea], [dev(b) for b in B],
+                            [dev(s) for s in eb], out, scale_kind=g.GEMMAR_SCALE_MX32, bands=Pm)
+        torch.cuda.synchronize()
+        assert g.gemmar_status(ctx)[0] == 0
+        rows = sample_rows(M, Pm, seed=5)
+        got = out[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+        ref, _ = oracle.gemm_reduce(A, ea, B, eb, 1, rows=rows)
+        check_bf16_output(got, ref, f"fused mx P=4 M={M} N={N} K={K}")
+        assert torch.isfinite(out.float()).all()
+    finally:
+        ctx.close()

@@ -171,3 +171,15 @@ def test_fused_fp8_wire(g, ctx):
     g.rowdequant_e4m3(ctx, q, s, y)
     status_ok(g, ctx)
     assert torch.equal(y.view(torch.int16), wire.view(torch.int16))
+
+
+@pytest.mark.parametrize("kind,P,M,N,K", [(0, 2, 256, 512, 256), (0, 3, 600, 384, 384), (0, 8, 512, 256, 128),
+                                          (1, 2, 256, 448, 256), (1, 3, 300, 256, 256)])
+def test_fused_slice_loop_vs_oracle_and_deterministic(g, ctx, kind, P, M, N, K):
+    ops = blockscale_operands(P, M, N, K, seed=11 + P) if kind == 0 else mx_operands(P, M, N, K, seed=11 + P)
+    A, sa, B, sb = ops
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, kind)
+    out1 = run_fused(g, ctx, A, sa, B, sb, kind, P, flags=g.GEMMAR_FUSE_SLICES | g.GEMMAR_DEBUG_CANARY)
+    out2 = run_fused(g, ctx, A, sa, B, sb, kind, P, flags=g.GEMMAR_FUSE_SLICES)
+    check_bf16_output(out1.float().cpu().numpy(), ref, f"slice loop kind={kind} P={P} M={M} N={N} K={K}")
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
