@@ -450,6 +450,41 @@ def run_ours(args, rank, world, local_rank):
     return 0
 
 
+def run_profile_case(args):
+    """One warm-up and one measured call of a single configuration, for
+    profilers (ncu -k ... -s 1 -c 1): the fused layer (blockscale P=8 or mx
+    P=4 at M rows, with --flags), or the row codec alone on a [M, 7168] bf16
+    matrix (--codec).  No timing is printed; the exit status is the device
+    status."""
+    import torch
+    import block_scaled_fp8_gemm_gb300 as g
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    M, N, K = args.m, N_HEAD, K_HEAD
+    kind = 1 if args.kind == "mx" else 0
+    P = 4 if kind == 1 else P_HEAD
+    ctx = g.gemmar_create(0, M, N, K, P, flags=g.GEMMAR_NO_SELF_TEST)
+    if args.codec:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(0)
+        x = torch.randn((M, N), generator=gen, device=dev).to(torch.bfloat16)
+        q = torch.empty((M, N), dtype=torch.uint8, device=dev)
+        s = torch.empty((M,), dtype=torch.float32, device=dev)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        for _ in range(2):
+            g.rowquant_e4m3(ctx, x, q, s)
+            g.rowdequant_e4m3(ctx, q, s, y)
+    else:
+        A, sa, B, sb = make_inputs(g, ctx, P, M, N, K, dev, seed=1, kind=kind)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        for _ in range(2):
+            g.fused_gemm_reduce(ctx, A, sa, B, sb, out, scale_kind=kind, bands=P, flags=args.flags)
+    torch.cuda.synchronize()
+    code, detail = g.gemmar_status(ctx)
+    ctx.close()
+    return 0 if code == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -457,7 +492,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle leg")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="single-shot case for profilers (see --kind, --m, --flags, --codec); prints nothing")
+    ap.add_argument("--kind", choices=("blockscale", "mx"), default="blockscale")
+    ap.add_argument("--m", type=int, default=2048)
+    ap.add_argument("--flags", type=int, default=0, help="fused_gemm_reduce flags (1 fp8 wire, 16 slice loop)")
+    ap.add_argument("--codec", action="store_true", help="profile case: the row codec alone on [M, 7168] bf16")
     args = ap.parse_args()
+    if args.profile_case:
+        return run_profile_case(args)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
