@@ -206,6 +206,40 @@ __device__ __forceinline__ uint32_t enc4(float a, float b, float c, float d, flo
     return lo | (hi << 16);
 }
 
+// e4m3 codes of RN(a/s) and RN(b/s) without dividing, given y = RN(1/s)
+// (s > 0 and 1/s finite).  q = a*y is within 3*2^-24 relative of a/s, and so
+// of RN(a/s); the products q*(1 -+ 2^-21) -- rounded -- still enclose that
+// neighbourhood.  Rounding to e4m3 (nearest-even, saturating) is monotone, so
+// when both ends give the same code every value between them does, RN(a/s)
+// included.  Otherwise (within ~2^-21 of a rounding midpoint) divide exactly.
+__device__ __forceinline__ uint32_t enc2_guarded(float a, float b, float s, float y)
+{
+    const float qa = __fmul_rn(a, y), qb = __fmul_rn(b, y);
+    const uint32_t lo = e4m3x2_from_f32(__fmul_rn(qa, 1.0f - 0x1p-21f), __fmul_rn(qb, 1.0f - 0x1p-21f));
+    const uint32_t hi = e4m3x2_from_f32(__fmul_rn(qa, 1.0f + 0x1p-21f), __fmul_rn(qb, 1.0f + 0x1p-21f));
+    if (lo == hi)
+        return lo;
+    return e4m3x2_from_f32(__fdiv_rn(a, s), __fdiv_rn(b, s));
+}
+
+// Row/group encoder: the guarded multiply when 1/s is a finite normal number,
+// exact division otherwise (s == 0 gives +0 codes).
+struct Enc {
+    float s, y;
+    bool fast;
+    __device__ __forceinline__ explicit Enc(float sc) : s(sc)
+    {
+        y = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+        fast = sc >= 0x1p-125f;   // 1/s < 2^125: finite, and q*(1+2^-21) cannot overflow
+    }
+    __device__ __forceinline__ uint32_t operator()(float a, float b, float c, float d) const
+    {
+        if (!fast)
+            return enc4(a, b, c, d, s);
+        return enc2_guarded(a, b, s, y) | (enc2_guarded(c, d, s, y) << 16);
+    }
+};
+
 template <bool BF16>
 __global__ void __launch_bounds__(256) rowquant_kernel(const void *__restrict__ x, int64_t M, int64_t N,
                                                        uint8_t *__restrict__ q, float *__restrict__ s)
@@ -229,13 +263,14 @@ __global__ void __launch_bounds__(256) rowquant_kernel(const void *__restrict__ 
         const float sc = __fdiv_rn(amax, 448.0f);
         if (lane == 0)
             s[row] = sc;
+        const Enc enc(sc);
 #pragma unroll 4
         for (int64_t c = (int64_t)lane * 8; c < N; c += 256) {
             float v[8];
             load8<BF16>(x, base + c, v);
             uint2 w;
-            w.x = enc4(v[0], v[1], v[2], v[3], sc);
-            w.y = enc4(v[4], v[5], v[6], v[7], sc);
+            w.x = enc(v[0], v[1], v[2], v[3]);
+            w.y = enc(v[4], v[5], v[6], v[7]);
             *reinterpret_cast<uint2 *>(q + base + c) = w;
         }
     }
@@ -279,12 +314,13 @@ __global__ void __launch_bounds__(256, 5) rowquant_bf16_cta_kernel(const uint16_
     const float sc = __fdiv_rn(amax, 448.0f);
     if (t == 0)
         s[row] = sc;
+    const Enc enc(sc);
     uint2 *qr = reinterpret_cast<uint2 *>(q + row * N);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         uint2 o;
-        o.x = enc4(bf16_lo(w[c].x), bf16_hi(w[c].x), bf16_lo(w[c].y), bf16_hi(w[c].y), sc);
-        o.y = enc4(bf16_lo(w[c].z), bf16_hi(w[c].z), bf16_lo(w[c].w), bf16_hi(w[c].w), sc);
+        o.x = enc(bf16_lo(w[c].x), bf16_hi(w[c].x), bf16_lo(w[c].y), bf16_hi(w[c].y));
+        o.y = enc(bf16_lo(w[c].z), bf16_hi(w[c].z), bf16_lo(w[c].w), bf16_hi(w[c].w));
         __stcs(qr + t + c * T, o);
     }
 }
@@ -308,26 +344,15 @@ __device__ __forceinline__ void dequant16(const uint4 c, float sc, uint16_t *y)
     __stcs(dst + 1, make_uint4(o[4], o[5], o[6], o[7]));
 }
 
-// 16 codes per pack; each thread keeps 4 packs (4 x 16-byte loads) in flight.
+// 16 codes per pack, one pack per thread per loop trip; the launch gives 16
+// blocks per SM, so the latency is covered by resident warps rather than by
+// deep per-thread unrolling (which throttled the load/store unit).
 __global__ void __launch_bounds__(256) rowdequant_kernel(const uint8_t *__restrict__ q, const float *__restrict__ s,
                                                          int64_t M, int64_t N, uint16_t *__restrict__ y)
 {
     const int64_t n16 = M * N / 16;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (; i + 3 * stride < n16; i += 4 * stride) {
-        uint4 c[4];
-        float sc[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            c[u] = __ldcs(reinterpret_cast<const uint4 *>(q + (i + u * stride) * 16));
-            sc[u] = __ldg(s + (i + u * stride) * 16 / N);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            dequant16(c[u], sc[u], y + (i + u * stride) * 16);
-    }
-    for (; i < n16; i += stride)
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
         dequant16(__ldcs(reinterpret_cast<const uint4 *>(q + i * 16)), __ldg(s + i * 16 / N), y + i * 16);
 }
 
@@ -354,7 +379,7 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const float *__restric
         const float sc = __fdiv_rn(amax, 448.0f);
         if (lane == 0)
             scales[gi] = sc;
-        *reinterpret_cast<uint32_t *>(q + e) = enc4(v.x, v.y, v.z, v.w, sc);
+        *reinterpret_cast<uint32_t *>(q + e) = Enc(sc)(v.x, v.y, v.z, v.w);
     }
 }
 
@@ -388,10 +413,11 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const float *__restr
         const float sc = __fdiv_rn(m, 448.0f);
         if (tid == 0)
             scales[bi] = sc;
+        const Enc enc(sc);
         for (int rr = warp; rr < rows; rr += 8) {
             const int64_t e = (r0 + rr) * C + bc * 128 + lane * 4;
             const float4 v = *reinterpret_cast<const float4 *>(x + e);
-            *reinterpret_cast<uint32_t *>(q + e) = enc4(v.x, v.y, v.z, v.w, sc);
+            *reinterpret_cast<uint32_t *>(q + e) = enc(v.x, v.y, v.z, v.w);
         }
         __syncthreads();
     }
@@ -569,7 +595,7 @@ cudaError_t launch_rowdequant(const uint8_t *q, const float *s, int64_t M, int64
                               cudaStream_t st)
 {
     const int64_t need = (M * N / 16 + 255) / 256;
-    const int grid = (int)max64(1, min64(need, (int64_t)num_sms * 8));
+    const int grid = (int)max64(1, min64(need, (int64_t)num_sms * 16));
     rowdequant_kernel<<<grid, 256, 0, st>>>(q, s, M, N, y);
     return cudaGetLastError();
 }
