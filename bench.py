@@ -379,25 +379,57 @@ def run_ours(args, rank, world, local_rank):
     del Amx, eam, Bmx, ebm
     torch.cuda.empty_cache()
 
-    # ---- end to end through the public API, inputs from pinned host memory
+    # ---- end to end through the public API: every step copies its activations
+    # (A codes + scales) from pinned host memory and reads its bf16 result back;
+    # the layer's weights stay resident, as in a served model.  Copies run on
+    # their own streams with double-buffered device tensors, so step i's
+    # compute overlaps step i+1's upload and step i-1's download.
     A, sa, B, sb = make_inputs(g, ctx, P, M, N, K, dev, seed=1 + rank, kind=0)
     hA = [a.cpu().pin_memory() for a in A]
     hsa = [s.cpu().pin_memory() for s in sa]
-    hB = [b.cpu().pin_memory() for b in B]
-    hsb = [s.cpu().pin_memory() for s in sb]
-    hout = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in hA + hsa + hB + hsb)
-    d2h = hout.numel() * hout.element_size()
+    hout = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dA = [A, [torch.empty_like(a) for a in A]]
+    dsa = [sa, [torch.empty_like(s) for s in sa]]
+    dout = [out, torch.empty_like(out)]
+    h2d = sum(t.numel() * t.element_size() for t in hA + hsa)
+    d2h = hout[0].numel() * hout[0].element_size()
+    s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    up_done, comp_done, down_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    for e in comp_done + down_done:
+        e.record(stream)
 
-    def e2e_step():
-        for dst, src in zip(A + sa + B + sb, hA + hsa + hB + hsb):
-            dst.copy_(src, non_blocking=True)
-        g.fused_gemm_reduce(ctx, A, sa, B, sb, out, bands=P)
-        hout.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        j = i & 1
+        with torch.cuda.stream(s_up):
+            s_up.wait_event(comp_done[j])            # the buffer set's previous compute is done
+            for dst, src in zip(dA[j] + dsa[j], hA + hsa):
+                dst.copy_(src, non_blocking=True)
+            up_done[j].record(s_up)
+        stream.wait_event(up_done[j])
+        stream.wait_event(down_done[j])               # the output buffer has been read back
+        g.fused_gemm_reduce(ctx, dA[j], dsa[j], B, sb, dout[j], bands=P)
+        comp_done[j].record(stream)
+        with torch.cuda.stream(s_down):
+            s_down.wait_event(comp_done[j])
+            hout[j].copy_(dout[j], non_blocking=True)
+            down_done[j].record(s_down)
 
-    for _ in range(2):
-        e2e_step()
-    e2e_ms = time_steps(e2e_step, max(3, args.steps // 4), stream)
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    n_e2e = max(4, args.steps // 4)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    s_up.wait_stream(stream)
+    s_down.wait_stream(stream)
+    for i in range(n_e2e):
+        e2e_step(i)
+    stream.wait_stream(s_up)
+    stream.wait_stream(s_down)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = t0.elapsed_time(t1) / n_e2e
     if world > 1:
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -440,7 +472,11 @@ def run_ours(args, rank, world, local_rank):
                             "frac_of_measured_hbm": reduce_gbs / peaks["hbm_gbs"]},
             **extra,
             "e2e": {"value": world * fl / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                    "us_per_layer": e2e_ms * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "us_per_layer": e2e_ms * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": n_e2e,
+                    "what": "per step: activations (A codes + 1x128 scales) host->device, fused_gemm_reduce, "
+                            "bf16 result device->host, all on the clock; weights resident; uploads and "
+                            "downloads on their own streams overlap the neighbouring steps' compute"},
             "gpu_launches": 2 * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
