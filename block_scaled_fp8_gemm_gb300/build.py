@@ -12,7 +12,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libgemmar.so")
-SOURCES = ["gemm_blockscale.cu", "gemm_mx.cu", "streaming.cu", "gemmar.cu", "noalloc.cu"]
+SOURCES = ["gemm_blockscale.cu", "gemm_blockscale_2sm.cu", "gemm_mx.cu", "streaming.cu", "gemmar.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

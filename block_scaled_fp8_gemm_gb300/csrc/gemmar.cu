@@ -133,7 +133,6 @@ int shape_rules(int P, int64_t M, int64_t N, int64_t K, int bands, int scale_kin
     return GEMMAR_OK;
 }
 
-int bs_tile_n(int64_t N) { return (N % 256 == 0) ? 256 : 128; }
 int mx_tile_n(int64_t N) { return (N % 224 == 0) ? 224 : 128; }
 
 TileGrid make_grid(int P, int64_t M, int64_t N, int64_t K, int bands, int bn, int slice_loop = 0)
@@ -185,23 +184,23 @@ int run_gemm(gemmar_ctx *ctx, int P, const uint8_t *const *A, const void *const 
     if (!load_encode())
         return GEMMAR_ERR_CUDA;
     if (scale_kind == GEMMAR_SCALE_BLOCK128) {
-        const int bn = bs_tile_n(N);
-        if (!register_split_ok(bn))
+        const BsPlan pl = plan_blockscale(P, M, N, K, bands, slice_loop, ctx->num_sms,
+                                          (ctx->flags & GEMMAR_CTA_PAIR) ? 1 : 0);
+        if (!pl.pair && !register_split_ok(pl.bn))
             return GEMMAR_ERR_DEVICE;
         BsParams prm;
         std::memset(&prm, 0, sizeof(prm));
         for (int p = 0; p < P; ++p) {
-            if (!make_tmap_u8(&prm.tmA[p], A[p], M, K, 128) || !make_tmap_u8(&prm.tmB[p], B[p], N, K, bn))
+            if (!make_tmap_u8(&prm.tmA[p], A[p], M, K, 128) || !make_tmap_u8(&prm.tmB[p], B[p], N, K, pl.box_b_rows))
                 return GEMMAR_ERR_CUDA;
             prm.sa[p] = static_cast<const float *>(sa[p]);
             prm.sb[p] = static_cast<const float *>(sb[p]);
         }
-        prm.g = make_grid(P, M, N, K, bands, bn, slice_loop);
+        prm.g = pl.g;
         prm.o = o;
         prm.status = ctx->status;
         prm.timeout_ns = ctx->timeout_ns;
-        const int grid = std::min(prm.g.num_tiles, ctx->num_sms);
-        CUDA_OK(launch_gemm_blockscale(prm, bn, grid, st));
+        CUDA_OK(launch_blockscale(prm, pl, st));
     } else {
         const int bn = mx_tile_n(N);
         if (slice_loop)
@@ -438,10 +437,18 @@ GEMMAR_API int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A
         if ((rc = run_gemm(ctx, P, A, sa, B, sb, scale_kind, M, N, K, bands, o, st)))
             return rc;
         mark(ctx, GEMMAR_PHASE_REDUCE, st);
-        const int bn = scale_kind == GEMMAR_SCALE_BLOCK128 ? bs_tile_n(N) : mx_tile_n(N);
-        const TileGrid g = make_grid(P, M, N, K, bands, bn);
-        // every epilogue warp (8 per tile) signals once per retired tile
-        const uint32_t expected = (uint32_t)(g.mt_per_band * g.ntiles_n * P * 8);
+        int bn;
+        uint32_t expected;   // every epilogue warp signals once per retired tile
+        if (scale_kind == GEMMAR_SCALE_BLOCK128) {
+            const BsPlan pl = plan_blockscale(P, M, N, K, bands, 0, ctx->num_sms,
+                                              (ctx->flags & GEMMAR_CTA_PAIR) ? 1 : 0);
+            bn = pl.bn;
+            expected = pl.band_signals;
+        } else {
+            bn = mx_tile_n(N);
+            const TileGrid g = make_grid(P, M, N, K, bands, bn);
+            expected = (uint32_t)(g.mt_per_band * g.ntiles_n * P * 8);
+        }
         CUDA_OK(launch_band_reduce_blocked(ctx->W, out, P, M, N, bands, bn, ctx->band_done, expected, ctx->status,
                                            ctx->timeout_ns, ctx->num_sms * 8, st));
     }

@@ -68,6 +68,25 @@ int gemm_blockscale_num_regs(int bn);
 int gemm_mx_num_regs(int bn);
 int gemm_threads();
 
+// Blockscale launch plan: CTA pairs (gemm_blockscale_2sm.cu, 256 x 128 pair
+// tiles) when the device can co-schedule two-CTA clusters, else one CTA per
+// tile (gemm_blockscale.cu, 128 x bn).  Every blockscale path of the library
+// goes through the same plan, so all of them share one arithmetic.
+struct BsPlan {
+    int pair;              // 1: CTA-pair kernel
+    int bn;                // tile width along N (also the blocked-partial tile width)
+    int box_b_rows;        // rows of B each CTA loads per stage (TMA box)
+    int grid;              // CTAs to launch
+    uint32_t band_signals; // release signals per band in the fused band path
+    TileGrid g;
+};
+BsPlan plan_blockscale(int P, int64_t M, int64_t N, int64_t K, int bands, int slice_loop, int num_sms,
+                       int use_pair = 0);
+cudaError_t launch_blockscale(const BsParams &p, const BsPlan &plan, cudaStream_t s);
+int gemm_blockscale_2sm_max_clusters();
+int gemm_blockscale_2sm_num_regs();
+cudaError_t launch_gemm_blockscale_2sm(const BsParams &p, int clusters, cudaStream_t s);
+
 // Scale repack for the mx GEMM (row-major ue8m0 bytes -> the tcgen05.cp image).
 // ea/eb are host arrays of P device pointers.  Image layout: see streaming.cu.
 cudaError_t launch_mx_repack(const uint8_t *const *ea, const uint8_t *const *eb, int P, int M, int N, int K,

@@ -128,29 +128,23 @@ extern "C" __attribute__((visibility("default"))) int fused_gemm_reduce_noalloc(
     int rc = scratch_for_device(device, &s);
     if (rc != GEMMAR_OK)
         return rc;
-    const int bn = (N % 256 == 0) ? 256 : 128;
-    const int regs = gemm_blockscale_num_regs(bn);
-    if (regs < 0 || (int64_t)regs * gemm_threads() < 56 * 128 + 224 * 256)
-        return GEMMAR_ERR_DEVICE;
+    const BsPlan pl = plan_blockscale(P, M, N, K, bands, 0, s->num_sms);
+    if (!pl.pair) {
+        const int regs = gemm_blockscale_num_regs(pl.bn);
+        if (regs < 0 || (int64_t)regs * gemm_threads() < 56 * 128 + 224 * 256)
+            return GEMMAR_ERR_DEVICE;
+    }
+    const int bn = pl.bn;
 
     BsParams prm;
     std::memset(&prm, 0, sizeof(prm));
     for (int p = 0; p < P; ++p) {
-        if (!tmap_u8(&prm.tmA[p], A[p], M, K, 128) || !tmap_u8(&prm.tmB[p], B[p], N, K, bn))
+        if (!tmap_u8(&prm.tmA[p], A[p], M, K, 128) || !tmap_u8(&prm.tmB[p], B[p], N, K, pl.box_b_rows))
             return GEMMAR_ERR_CUDA;
         prm.sa[p] = sa[p];
         prm.sb[p] = sb[p];
     }
-    TileGrid &g = prm.g;
-    g.P = P;
-    g.M = (int)M;
-    g.N = (int)N;
-    g.K = (int)K;
-    g.bands = bands;
-    g.rows_per_band = (int)(M / bands);
-    g.mt_per_band = (g.rows_per_band + 127) / 128;
-    g.ntiles_n = (int)(N / bn);
-    g.num_tiles = bands * P * g.mt_per_band * g.ntiles_n;
+    prm.g = pl.g;
     prm.o = GemmOut{s->partials, s->band_done, OUT_PARTIAL_F32, -1};
     prm.status = s->status;
     prm.timeout_ns = kTimeoutNs;
@@ -160,9 +154,9 @@ extern "C" __attribute__((visibility("default"))) int fused_gemm_reduce_noalloc(
     if (cudaMemsetAsync(s->band_done, 0, sizeof(uint32_t) * bands, st) != cudaSuccess ||
         cudaMemsetAsync(s->status, 0, sizeof(ptx::DevStatus), st) != cudaSuccess)
         return GEMMAR_ERR_CUDA;
-    if (launch_gemm_blockscale(prm, bn, g.num_tiles < s->num_sms ? g.num_tiles : s->num_sms, st) != cudaSuccess)
+    if (launch_blockscale(prm, pl, st) != cudaSuccess)
         return GEMMAR_ERR_CUDA;
-    const uint32_t expected = (uint32_t)(g.mt_per_band * g.ntiles_n * P * 8);
+    const uint32_t expected = pl.band_signals;
     if (launch_band_reduce_blocked(s->partials, out, P, M, N, bands, bn, s->band_done, expected, s->status,
                                    kTimeoutNs, s->num_sms * 8, st) != cudaSuccess)
         return GEMMAR_ERR_CUDA;

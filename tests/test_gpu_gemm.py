@@ -183,3 +183,51 @@ def test_fused_slice_loop_vs_oracle_and_deterministic(g, ctx, kind, P, M, N, K):
     out2 = run_fused(g, ctx, A, sa, B, sb, kind, P, flags=g.GEMMAR_FUSE_SLICES)
     check_bf16_output(out1.float().cpu().numpy(), ref, f"slice loop kind={kind} P={P} M={M} N={N} K={K}")
     assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
+# ------------------------------------------------------------ CTA-pair vs one-CTA kernel
+
+@pytest.fixture(scope="module")
+def ctx_pair(g):
+    torch.cuda.set_device(0)
+    c = g.gemmar_create(0, 1024, 1024, 512, 8, flags=g.GEMMAR_NO_SELF_TEST | g.GEMMAR_CTA_PAIR,
+                        wait_timeout_ns=1_000_000_000)
+    yield c
+    c.close()
+
+
+@pytest.mark.parametrize("P,M,N,K,bands", [(2, 256, 512, 256, 2), (3, 600, 384, 384, 3), (8, 1024, 256, 128, 8),
+                                           (4, 520, 640, 256, 4)])
+def test_pair_and_single_cta_kernels_agree(g, ctx, ctx_pair, P, M, N, K, bands):
+    A, sa, B, sb = blockscale_operands(P, M, N, K, seed=P * M + 3)
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, 0)
+    pair = run_fused(g, ctx_pair, A, sa, B, sb, 0, bands, flags=g.GEMMAR_DEBUG_CANARY)
+    one = run_fused(g, ctx, A, sa, B, sb, 0, bands, flags=g.GEMMAR_DEBUG_CANARY)
+    check_bf16_output(pair.float().cpu().numpy(), ref, f"pair kernel P={P} M={M} N={N} K={K}")
+    check_bf16_output(one.float().cpu().numpy(), ref, f"one-CTA kernel P={P} M={M} N={N} K={K}")
+    # the same fp32 promotion order on both: outputs differ by at most one bf16 ulp
+    a = pair.view(torch.int16).int()
+    b = one.view(torch.int16).int()
+    assert int((a - b).abs().max()) <= 1
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 384, 512), (1, 128, 128), (384, 768, 384)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_pair_gemm_blockscale(g, ctx_pair, M, N, K, out_dtype):
+    A, sa, B, sb = blockscale_operands(1, M, N, K, seed=M + 2 * N)
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, 0)
+    out = torch.full((M, N), float("nan"), dtype=out_dtype, device="cuda")
+    g.gemm_blockscale_fp8(ctx_pair, dev(A[0]), dev(sa[0]), dev(B[0]), dev(sb[0]), out)
+    status_ok(g, ctx_pair)
+    if out_dtype == torch.float32:
+        check_f32_output(out.cpu().numpy(), ref, f"pair blockscale f32 M={M} N={N} K={K}")
+    else:
+        check_bf16_output(out.float().cpu().numpy(), ref, f"pair blockscale bf16 M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("P,M,N,K", [(2, 256, 512, 256), (3, 600, 384, 384)])
+def test_pair_slice_loop(g, ctx_pair, P, M, N, K):
+    A, sa, B, sb = blockscale_operands(P, M, N, K, seed=31 + P)
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, 0)
+    out = run_fused(g, ctx_pair, A, sa, B, sb, 0, P, flags=g.GEMMAR_FUSE_SLICES | g.GEMMAR_DEBUG_CANARY)
+    check_bf16_output(out.float().cpu().numpy(), ref, f"pair slice loop P={P} M={M} N={N} K={K}")
