@@ -52,6 +52,7 @@ GEMMAR_FAULT_SKIP_BAND = 1 << 2
 GEMMAR_NO_SELF_TEST = 1 << 3
 GEMMAR_FUSE_SLICES = 1 << 4
 GEMMAR_CTA_PAIR = 1 << 5
+GEMMAR_FUSE_ONCHIP = 1 << 6
 GEMMAR_MAX_P = 8
 GEMMAR_NOALLOC_MAX_PARTIALS = 8 * 1024 * 1024
 

@@ -116,7 +116,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
                     mbar_arrive_expect_tx(full + stage, C::kStageBytes);
                     tma_load_2d(smem + C::kOffA + stage * C::kABytes, &prm.tmA[p], full + stage, kb * 128, tc.m0);
                     tma_load_2d(smem + C::kOffB + stage * C::kBBytes, &prm.tmB[p], full + stage, kb * 128, tc.n0);
-                    ++issued;
                     if (++stage == C::kStages) {
                         stage = 0;
                         ph ^= 1;
@@ -198,13 +197,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
 #pragma unroll
             for (int j = 0; j < HALF; ++j)
                 acc[j] = 0.0f;
-            // scales of the tile's K-steps, slice by slice: sa[p][row, kb] * sb[p][n/128, kb],
-            // each loaded one step ahead
+            // scales of the tile's K-steps, slice by slice: sa[p][row, kb] * sb[p][n/128, kb].
+            // The two factors are loaded a step ahead and multiplied where used, so
+            // the load latency overlaps the wait and the TMEM reads of a step.
             const float *sa_row = prm.sa[tc.p] + mrow * KB;
             const float *sb_blk = prm.sb[tc.p] + nblk * KB;
-            float s_next = __ldg(sa_row) * __ldg(sb_blk);
+            float a_next = __ldg(sa_row), b_next = __ldg(sb_blk);
             for (int ks = 0, sl = 0, kb = 0; ks < NKS; ++ks) {
-                const float s = s_next;
+                const float a_cur = a_next, b_cur = b_next;
                 if (++kb == KB) {
                     kb = 0;
                     if (++sl < nsl) {
@@ -212,14 +212,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
                         sb_blk = prm.sb[sl] + nblk * KB;
                     }
                 }
-                if (ks + 1 < NKS)
-                    s_next = __ldg(sa_row + kb) * __ldg(sb_blk + kb);
+                if (ks + 1 < NKS) {
+                    a_next = __ldg(sa_row + kb);
+                    b_next = __ldg(sb_blk + kb);
+                }
                 const uint32_t buf = kiter & 1, tph = (kiter >> 1) & 1;
                 if (!mbar_wait(tfull + buf, tph, abort_flag, prm.status, prm.timeout_ns, SITE_EPI_TMEM_FULL)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                const float s = a_cur * b_cur;
                 const uint32_t taddr = lane_base + buf * BN;
                 // 64 columns per TMEM load: the buffer is free again after
                 // HALF/64 load round trips, before the last 64 promotions.

@@ -3,21 +3,26 @@
 // All-Reduce Benchmark", "Running the benchmark": A 1x128, B 128x128 fp32
 // scales, applied per 128-K block while draining TMEM).
 //
-// A cluster of two CTAs on two SMs computes a 256 x 128 pair tile: CTA r owns
-// rows m0 + 128r .. +127 in its TMEM, loads those 128 rows of A and rows
-// n0 + 64r .. +63 of B into its shared memory (24 KB per 128-K stage, 8
-// stages), and the leader (rank 0) issues tcgen05.mma.cta_group::2 (M=256,
-// N=128, K=32) that reads both CTAs' stages.  Per SM that is the operand
-// traffic of a 128 x 256 single-CTA tile for half the TMEM, so:
-//   - TMEM holds 4 K-block buffers of 128 columns (4-deep MMA/epilogue slack);
-//   - each epilogue thread owns one row x 64 columns: acc[64] in registers,
-//     leaving room to park a finished tile's fp32 partial in registers and
-//     stream it to HBM one 16-byte unit per K-step of the next tile, so the
-//     partial write of the band path overlaps the tensor cores instead of
-//     stalling them.
-// Barriers: stage-full counts both CTAs' TMA bytes on the leader; stage-empty,
-// TMEM-full and the final barrier are multicast-committed to both CTAs;
-// TMEM-empty lives on the leader and collects 8 local + 8 remote arrivals.
+// A cluster of two CTAs on the two SMs of a TPC computes a 256 x 256 pair
+// tile: CTA r owns rows m0 + 128r .. +127 (all 256 columns) in its TMEM, and
+// per 128-K stage loads those 128 rows of A and rows n0 + 128r .. +127 of B
+// (32 KB); the leader (rank 0) issues tcgen05.mma.cta_group::2 (M=256, N=256,
+// K=32) reading both CTAs' stages.  Per SM that is the MMA shape of the
+// one-CTA 128 x 256 tile with half of its B traffic, which frees the shared
+// memory for what limits the one-CTA kernel on the band path: the tile's fp32
+// partial (128 KB per SM) is parked in shared memory at tile end and leaves
+// through one bulk asynchronous copy per warp while the next tile computes,
+// instead of stalling the epilogue on 128 KB of global stores.
+//
+// Per CTA:
+//   warp 0       TMA producer: 3 stages of 16 KB A + 16 KB B
+//   warp 1       TMEM allocation (both CTAs); MMA issue (leader only: the
+//                whole warp runs the loop, lane 0 polls, one lane issues)
+//   warps 4-11   epilogue: thread = one row x 128 columns (2 TMEM loads of 64
+//                per K-step), promotion acc += (sa * sb) * P_kb, tile store
+// Barriers: stage-full counts both CTAs' TMA bytes on the leader; stage-empty
+// and TMEM-full are multicast-committed to both CTAs; TMEM-empty lives on the
+// leader and collects 8 local + 8 remote arrivals.
 #include <algorithm>
 
 #include "epilogue.cuh"
@@ -28,21 +33,21 @@ using namespace ptx;
 namespace {
 
 constexpr int kThreads = 384;
-constexpr int kStages = 8;
+constexpr int kStages = 3;
 constexpr int kABytes = 128 * 128;           // this CTA's 128 rows of A, one 128-K stage
-constexpr int kBBytes = 64 * 128;            // this CTA's 64 rows of B
+constexpr int kBBytes = 128 * 128;           // this CTA's 128 rows of B
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kBufs = 4;                     // TMEM K-block buffers of 128 columns
+constexpr int kBufs = 2;                     // TMEM K-block buffers of 256 columns
 constexpr int kEpiWarps = 8;
+constexpr int kParkBytes = 16384;            // per epilogue warp: 32 rows x 128 fp32
 constexpr int kOffA = 0;
 constexpr int kOffB = kStages * kABytes;
-constexpr int kOffStaging = kOffB + kStages * kBBytes;
-constexpr int kOffBar = kOffStaging + kEpiWarps * 4096;
+constexpr int kOffPark = kOffB + kStages * kBBytes;
+constexpr int kOffBar = kOffPark + kEpiWarps * kParkBytes;
 constexpr int kNumBars = 2 * kStages + 2 * kBufs + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kBBytes % 1024 == 0, "B stages stay 1024-byte aligned");
 constexpr int kRegsLow = 56;
 constexpr int kRegsHigh = 224;
 constexpr uint32_t kAbortGraceNs = 200000;   // let in-flight copies land before an aborting CTA exits
@@ -56,7 +61,7 @@ __device__ __forceinline__ PairTile decode_pair(int t, const TileGrid &g)
     PairTile c;
     const int nt = t % g.ntiles_n;
     int r = t / g.ntiles_n;
-    c.n0 = nt * 128;
+    c.n0 = nt * 256;
     if (g.slice_loop) {
         c.b = 0;
         c.p = 0;
@@ -73,6 +78,21 @@ __device__ __forceinline__ PairTile decode_pair(int t, const TileGrid &g)
     c.band_end = min((c.b + 1) * g.rows_per_band, g.M);
     return c;
 }
+
+// Bulk asynchronous copy shared -> global (16-byte aligned, size % 16 == 0),
+// tracked in this thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void *gdst, uint32_t ssrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Every bulk group of this thread complete (writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Generic-proxy shared-memory writes visible to the async proxy (bulk copies).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Async-proxy global writes ordered before this thread's later generic accesses.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const __grid_constant__ BsParams prm)
 {
@@ -128,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const 
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------ TMA producer (both CTAs)
             const uint32_t full_leader = mapa_shared(smem_u32(full), 0);
-            int stage = 0, issued = 0;
+            int stage = 0;
             uint32_t ph = 0;
             bool ok = true;
             for (int t = cluster; t < g.num_tiles && ok; t += nclusters) {
@@ -144,22 +164,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const 
                     if (rank == 0)
                         mbar_arrive_expect_tx(full + stage, 2 * kStageBytes);
                     const uint32_t fb = full_leader + 8u * stage;
-                    tma_load_2d_pair(smem + kOffA + stage * kABytes, &prm.tmA[p], fb, kb * 128, tc.m0 + 128 * (int)rank);
-                    tma_load_2d_pair(smem + kOffB + stage * kBBytes, &prm.tmB[p], fb, kb * 128, tc.n0 + 64 * (int)rank);
-                    ++issued;
+                    tma_load_2d_pair(smem + kOffA + stage * kABytes, &prm.tmA[p], fb, kb * 128,
+                                     tc.m0 + 128 * (int)rank);
+                    tma_load_2d_pair(smem + kOffB + stage * kBBytes, &prm.tmB[p], fb, kb * 128,
+                                     tc.n0 + 128 * (int)rank);
                     if (++stage == kStages) {
                         stage = 0;
                         ph ^= 1;
                     }
                 }
             }
-            (void)issued;
         } else if (warp == 1 && rank == 0) {
             // ------------------------------------------------ MMA issuer (leader)
             // The whole warp runs the loop so that descriptors and TMEM addresses
             // stay warp-uniform; lane 0 polls the barriers and broadcasts the
             // outcome, one elected lane issues.
-            const uint32_t idesc = idesc_f8_e4m3(256, 128);
+            const uint32_t idesc = idesc_f8_e4m3(256, 256);
             int stage = 0;
             uint32_t ph = 0, kiter = 0;
             bool ok = true;
@@ -180,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const 
                     if (elect_one()) {
                         const uint64_t ad = desc_kmajor_sw128(smem_u32(smem + kOffA + stage * kABytes));
                         const uint64_t bd = desc_kmajor_sw128(smem_u32(smem + kOffB + stage * kBBytes));
-                        const uint32_t d = tmem_base + buf * 128;
+                        const uint32_t d = tmem_base + buf * 256;
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
                             mma_f8_pair(d, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
@@ -204,68 +224,59 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const 
         // ---------------------------------------------------- epilogue (both CTAs)
         const int ew = warp - 4;
         const int q = warp & 3;         // TMEM lane quarter
-        const int h = ew >> 2;          // 64-column half of the pair tile
+        const int h = ew >> 2;          // 128-column half of the CTA's 256 columns
         const int row = q * 32 + lane;  // row within this CTA's 128 rows
-        const uint32_t staging = smem_u32(smem + kOffStaging + ew * 4096);
-        const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + h * 64;
+        const uint32_t park = smem_u32(smem + kOffPark + ew * kParkBytes);
+        const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + h * 128;
         const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
         const bool partial = prm.o.out_mode == OUT_PARTIAL_F32;
-        // the previous tile's fp32 partial, stored one unit per K-step
-        float park[64];
-        float4 *park_base = nullptr;   // null: nothing parked
-        int park_band = 0;
+        const bool exact = g.slice_loop == 2;
+        int pend_band = -1;   // band of the partial whose bulk copy is in flight
         uint32_t kiter = 0;
         bool ok = true;
+        const int nsl = g.slice_loop ? g.P : 1;
         for (int t = cluster; t < g.num_tiles && ok; t += nclusters) {
             const PairTile tc = decode_pair(t, g);
             const int m_cta = tc.m0 + 128 * (int)rank;
             const int rows_valid = max(0, min(32, tc.band_end - m_cta - q * 32));
             const int64_t mrow = min(m_cta + row, g.M - 1);
-            const int64_t nblk = tc.n0 >> 7;
-            float acc[64];
+            const int64_t nblk = (tc.n0 + h * 128) >> 7;
+            float acc[128];
 #pragma unroll
-            for (int j = 0; j < 64; ++j)
+            for (int j = 0; j < 128; ++j)
                 acc[j] = 0.0f;
-            const int nsl = g.slice_loop ? g.P : 1;
+            // raw scale factors of the next K-step, loaded a step ahead and
+            // multiplied where used, so the load latency overlaps a step
             const float *sa_row = prm.sa[tc.p] + mrow * KB;
             const float *sb_blk = prm.sb[tc.p] + nblk * KB;
-            // raw scale factors of the next K-step, loaded a step ahead and
-            // multiplied only where used, so the load latency overlaps a step
             float a_next = __ldg(sa_row), b_next = __ldg(sb_blk);
-            int sl = 0, kb = 0;
-            for (int ks0 = 0; ks0 < NKS && ok; ks0 += 16) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    if (ks0 == 0 && park_base != nullptr) {
-                        // stream unit j of the parked partial (chunk h*2 + j/8, unit j%8)
-                        __stcg(park_base + ((q * 4 + h * 2 + (j >> 3)) * 8 + (j & 7)) * 32 + lane,
-                               make_float4(park[4 * j], park[4 * j + 1], park[4 * j + 2], park[4 * j + 3]));
-                        if (j == 15) {
-                            signal_band(prm.o, park_band);
-                            park_base = nullptr;
-                        }
+            for (int sl = 0; sl < nsl && ok; ++sl) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    const float a_cur = a_next, b_cur = b_next;
+                    if (kb + 1 < KB) {
+                        a_next = __ldg(sa_row + kb + 1);
+                        b_next = __ldg(sb_blk + kb + 1);
+                    } else if (sl + 1 < nsl) {
+                        sa_row = prm.sa[sl + 1] + mrow * KB;
+                        sb_blk = prm.sb[sl + 1] + nblk * KB;
+                        a_next = __ldg(sa_row);
+                        b_next = __ldg(sb_blk);
                     }
-                    if (ks0 + j < NKS && ok) {
-                        const float a_cur = a_next, b_cur = b_next;
-                        if (++kb == KB) {
-                            kb = 0;
-                            if (++sl < nsl) {
-                                sa_row = prm.sa[sl] + mrow * KB;
-                                sb_blk = prm.sb[sl] + nblk * KB;
-                            }
-                        }
-                        if (ks0 + j + 1 < NKS) {
-                            a_next = __ldg(sa_row + kb);
-                            b_next = __ldg(sb_blk + kb);
-                        }
-                        const uint32_t buf = kiter % kBufs, tph = (kiter / kBufs) & 1;
-                        if (!mbar_wait(tfull + buf, tph, abort_flag, prm.status, prm.timeout_ns, SITE_EPI_TMEM_FULL)) {
-                            ok = false;
-                        } else {
-                            tc_fence_after();
-                            uint32_t r[64];
-                            tmem_ld_x64(lane_base + buf * 128, r);
-                            tmem_wait_ld(r);
+                    const uint32_t buf = kiter % kBufs, tph = (kiter / kBufs) & 1;
+                    if (!mbar_wait(tfull + buf, tph, abort_flag, prm.status, prm.timeout_ns, SITE_EPI_TMEM_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const float s = a_cur * b_cur;
+                    const uint32_t taddr = lane_base + buf * 256;
+                    uint32_t r[64];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        tmem_ld_x64(taddr + c * 64, r);
+                        tmem_wait_ld(r);
+                        if (c == 1) {
+                            // the K-block buffer is read: hand it back to the MMA warp
                             tc_fence_before();
                             __syncwarp();
                             if (lane == 0) {
@@ -274,52 +285,106 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const 
                                 else
                                     mbar_arrive_cluster(tempty_leader + 8u * buf);
                             }
-                            const float s = a_cur * b_cur;
-#pragma unroll
-                            for (int i = 0; i < 64; i += 2)
-                                fma2(acc[i], acc[i + 1], s, r[i], r[i + 1]);
-                            ++kiter;
                         }
+#pragma unroll
+                        for (int j = 0; j < 64; j += 2)
+                            fma2(acc[c * 64 + j], acc[c * 64 + j + 1], s, r[j], r[j + 1]);
                     }
+                    ++kiter;
+                }
+                if (exact && ok && nsl > 1) {
+                    // acc is slice sl's fp32 partial W_sl of this row.  Fold it into
+                    // the running sum in the reducer's order, run = W_0 then
+                    // run = run + W_p; the last sum stays in acc.
+                    if (sl == 0) {
+#pragma unroll
+                        for (int u = 0; u < 32; ++u)
+                            st_shared_v4(park + (uint32_t)((u * 32 + lane) * 16),
+                                         make_uint4(__float_as_uint(acc[4 * u]), __float_as_uint(acc[4 * u + 1]),
+                                                    __float_as_uint(acc[4 * u + 2]), __float_as_uint(acc[4 * u + 3])));
+                    } else {
+                        const bool last = sl + 1 == nsl;
+#pragma unroll
+                        for (int u = 0; u < 32; ++u) {
+                            const uint32_t addr = park + (uint32_t)((u * 32 + lane) * 16);
+                            const uint4 v = ld_shared_v4(addr);
+                            acc[4 * u] = __fadd_rn(__uint_as_float(v.x), acc[4 * u]);
+                            acc[4 * u + 1] = __fadd_rn(__uint_as_float(v.y), acc[4 * u + 1]);
+                            acc[4 * u + 2] = __fadd_rn(__uint_as_float(v.z), acc[4 * u + 2]);
+                            acc[4 * u + 3] = __fadd_rn(__uint_as_float(v.w), acc[4 * u + 3]);
+                            if (!last)
+                                st_shared_v4(addr, make_uint4(__float_as_uint(acc[4 * u]), __float_as_uint(acc[4 * u + 1]),
+                                                              __float_as_uint(acc[4 * u + 2]),
+                                                              __float_as_uint(acc[4 * u + 3])));
+                        }
+                        if (last)
+                            continue;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 128; ++j)
+                        acc[j] = 0.0f;
                 }
             }
             if (!ok)
                 break;
+            __syncwarp();   // every lane's last read of the running sum precedes the staging writes
             // -------- tile store
             if (partial) {
-                // park this tile's partial; it goes out during the next tile's K-steps
-                if (park_base != nullptr) {   // a previous park not fully streamed (cannot happen: 16 units per first block)
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        __stcg(park_base + ((q * 4 + h * 2 + (j >> 3)) * 8 + (j & 7)) * 32 + lane,
-                               make_float4(park[4 * j], park[4 * j + 1], park[4 * j + 2], park[4 * j + 3]));
-                    signal_band(prm.o, park_band);
+                // The previous partial's copy has had a whole tile to land: wait for
+                // it (which also frees the park), then publish its band.
+                if (lane == 0) {
+                    bulk_wait_all();
+                    fence_proxy_async_global();
                 }
+                if (pend_band >= 0)
+                    signal_band(prm.o, pend_band);
+                __syncwarp();
+                pend_band = -1;
+                if (m_cta < tc.band_end) {
+                    // park this warp's 32 rows x 128 columns in the blocked order of the
+                    // partial layout (chunks h*4 .. h*4+3 of lane quarter q are 16 KB
+                    // contiguous in W), then one bulk copy takes it to HBM
 #pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    park[j] = acc[j];
-                park_band = tc.b;
-                const TileCoord ct{tc.b, tc.p, m_cta, tc.n0, 0};
-                // a CTA tile past the band end (ragged bands) owns no partial block
-                park_base = (m_cta < tc.band_end) ? partial_tile_base(prm.o, g, ct, 128) : nullptr;
-                if (park_base == nullptr)
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const float *a = &acc[c * 32 + u * 4];
+                            st_shared_v4(park + (uint32_t)(((c * 8 + u) * 32 + lane) * 16),
+                                         make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]),
+                                                    __float_as_uint(a[2]), __float_as_uint(a[3])));
+                        }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const TileCoord ct{tc.b, tc.p, m_cta, tc.n0, 0};
+                        float4 *tb = partial_tile_base(prm.o, g, ct, 256);
+                        bulk_store(tb + ((q * 8 + h * 4) * 8) * 32, park, (uint32_t)kParkBytes);
+                        bulk_commit();
+                    }
+                    pend_band = tc.b;
+                } else {
+                    // a CTA tile past the band end (ragged bands) owns no partial block
                     signal_band(prm.o, tc.b);
+                }
             } else if (prm.o.out_mode == OUT_BF16) {
                 const TileCoord ct{tc.b, tc.p, m_cta, tc.n0, 0};
-                char *base = tile_out_base(prm.o, g, ct, 2) + ((int64_t)q * 32 * g.N + h * 64) * 2;
-                uint4 v[8];
+                char *base = tile_out_base(prm.o, g, ct, 2) + ((int64_t)q * 32 * g.N + h * 128) * 2;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const float *a = &acc[u * 8];
-                    v[u] = make_uint4(bf16x2_from_f32(a[0], a[1]), bf16x2_from_f32(a[2], a[3]),
-                                      bf16x2_from_f32(a[4], a[5]), bf16x2_from_f32(a[6], a[7]));
+                for (int c = 0; c < 4; ++c) {
+                    uint4 v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float *a = &acc[c * 32 + u * 8];
+                        v[u] = make_uint4(bf16x2_from_f32(a[0], a[1]), bf16x2_from_f32(a[2], a[3]),
+                                          bf16x2_from_f32(a[4], a[5]), bf16x2_from_f32(a[6], a[7]));
+                    }
+                    store_chunk<4>(park, v, base + c * 64, (int64_t)g.N * 2, rows_valid);
                 }
-                store_chunk<8>(staging, v, base, (int64_t)g.N * 2, rows_valid);
             } else {
                 const TileCoord ct{tc.b, tc.p, m_cta, tc.n0, 0};
-                char *base = tile_out_base(prm.o, g, ct, 4) + ((int64_t)q * 32 * g.N + h * 64) * 4;
+                char *base = tile_out_base(prm.o, g, ct, 4) + ((int64_t)q * 32 * g.N + h * 128) * 4;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     uint4 v[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
@@ -327,18 +392,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const 
                         v[u] = make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
                                           __float_as_uint(a[3]));
                     }
-                    store_chunk<8>(staging, v, base + c * 128, (int64_t)g.N * 4, rows_valid);
+                    store_chunk<8>(park, v, base + c * 128, (int64_t)g.N * 4, rows_valid);
                 }
             }
         }
-        // the last parked partial
-        if (ok && park_base != nullptr) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                __stcg(park_base + ((q * 4 + h * 2 + (j >> 3)) * 8 + (j & 7)) * 32 + lane,
-                       make_float4(park[4 * j], park[4 * j + 1], park[4 * j + 2], park[4 * j + 3]));
-            signal_band(prm.o, park_band);
+        // the last partial: its copy completes before the band is published and
+        // before the shared memory it reads from is released
+        if (lane == 0) {
+            bulk_wait_all();
+            fence_proxy_async_global();
         }
+        if (ok && pend_band >= 0)
+            signal_band(prm.o, pend_band);
     }
 
     __syncwarp();
@@ -421,25 +486,28 @@ BsPlan plan_blockscale(int P, int64_t M, int64_t N, int64_t K, int bands, int sl
     g.rows_per_band = (int)(M / bands);
     g.mt_per_band = (g.rows_per_band + 127) / 128;   // 128-row tiles of the blocked partial layout
     g.slice_loop = slice_loop;
-    const int regs2 = gemm_blockscale_2sm_num_regs();
-    const int clusters = gemm_blockscale_2sm_max_clusters();
-    pl.pair = use_pair && clusters > 0 && regs2 >= 0 && (int64_t)regs2 * gemm_threads() >= 56 * 128 + 224 * 256;
-    if (pl.pair) {
-        pl.bn = 128;
-        pl.box_b_rows = 64;
-        g.ntiles_n = (int)(N / 128);
-        const int mt2 = (g.rows_per_band + 255) / 256;
-        g.num_tiles = (slice_loop ? 1 : P) * bands * mt2 * g.ntiles_n;
-        pl.grid = 2 * std::min(g.num_tiles, clusters);
-        pl.band_signals = (uint32_t)(mt2 * g.ntiles_n * P * 16);   // 8 warps x 2 CTAs per pair tile
-    } else {
-        pl.bn = (N % 256 == 0) ? 256 : 128;
-        pl.box_b_rows = pl.bn;
-        g.ntiles_n = (int)(N / pl.bn);
-        g.num_tiles = (slice_loop ? 1 : P) * bands * g.mt_per_band * g.ntiles_n;
-        pl.grid = std::min(g.num_tiles, num_sms);
-        pl.band_signals = (uint32_t)(g.mt_per_band * g.ntiles_n * P * 8);
+    if (use_pair && N % 256 == 0) {
+        const int regs2 = gemm_blockscale_2sm_num_regs();
+        const int clusters = gemm_blockscale_2sm_max_clusters();
+        if (clusters > 0 && regs2 >= 0 && (int64_t)regs2 * gemm_threads() >= 56 * 128 + 224 * 256) {
+            pl.pair = 1;
+            pl.bn = 256;
+            pl.box_b_rows = 128;
+            g.ntiles_n = (int)(N / 256);
+            const int mt2 = (g.rows_per_band + 255) / 256;
+            g.num_tiles = (slice_loop ? 1 : P) * bands * mt2 * g.ntiles_n;
+            pl.grid = 2 * std::min(g.num_tiles, clusters);
+            pl.band_signals = (uint32_t)(mt2 * g.ntiles_n * P * 16);   // 8 warps x 2 CTAs per pair tile
+            return pl;
+        }
     }
+    pl.pair = 0;
+    pl.bn = (N % 256 == 0) ? 256 : 128;
+    pl.box_b_rows = pl.bn;
+    g.ntiles_n = (int)(N / pl.bn);
+    g.num_tiles = (slice_loop ? 1 : P) * bands * g.mt_per_band * g.ntiles_n;
+    pl.grid = std::min(g.num_tiles, num_sms);
+    pl.band_signals = (uint32_t)(g.mt_per_band * g.ntiles_n * P * 8);
     return pl;
 }
 

@@ -184,8 +184,11 @@ int run_gemm(gemmar_ctx *ctx, int P, const uint8_t *const *A, const void *const 
     if (!load_encode())
         return GEMMAR_ERR_CUDA;
     if (scale_kind == GEMMAR_SCALE_BLOCK128) {
+        // slice_loop 2 (partials summed on chip) exists on the CTA-pair kernel only
         const BsPlan pl = plan_blockscale(P, M, N, K, bands, slice_loop, ctx->num_sms,
-                                          (ctx->flags & GEMMAR_CTA_PAIR) ? 1 : 0);
+                                          (slice_loop == 2 || (ctx->flags & GEMMAR_CTA_PAIR)) ? 1 : 0);
+        if (slice_loop == 2 && !pl.pair)
+            return GEMMAR_ERR_DEVICE;
         if (!pl.pair && !register_split_ok(pl.bn))
             return GEMMAR_ERR_DEVICE;
         BsParams prm;
@@ -411,7 +414,11 @@ GEMMAR_API int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A
     }
     if (!aligned16(out))
         return GEMMAR_ERR_ALIGN;
-    const bool slices = (flags & GEMMAR_FUSE_SLICES) != 0;
+    // on-chip partial sums: blockscale on the CTA-pair kernel; elsewhere the band path,
+    // whose bits it reproduces
+    const bool onchip = (flags & GEMMAR_FUSE_ONCHIP) && scale_kind == GEMMAR_SCALE_BLOCK128 &&
+                        plan_blockscale(P, M, N, K, bands, 2, ctx->num_sms, 1).pair;
+    const bool slices = onchip || ((flags & GEMMAR_FUSE_SLICES) != 0 && !(flags & GEMMAR_FUSE_ONCHIP));
     if (!slices && blocked_partial_floats(P, M, bands, N) > ctx->W_floats)
         return GEMMAR_ERR_WORKSPACE;
     if ((flags & GEMMAR_FP8_WIRE) && M * N > ctx->max_M * ctx->N)
@@ -423,7 +430,7 @@ GEMMAR_API int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A
             CUDA_OK(cudaMemsetAsync(out, 0xFF, sizeof(uint16_t) * (size_t)(M * N), st));
         mark(ctx, GEMMAR_PHASE_GEMM, st);
         GemmOut os{out, nullptr, OUT_BF16, -1};
-        if ((rc = run_gemm(ctx, P, A, sa, B, sb, scale_kind, M, N, K, 1, os, st, 1)))
+        if ((rc = run_gemm(ctx, P, A, sa, B, sb, scale_kind, M, N, K, 1, os, st, onchip ? 2 : 1)))
             return rc;
         mark(ctx, GEMMAR_PHASE_REDUCE, st);
     } else {

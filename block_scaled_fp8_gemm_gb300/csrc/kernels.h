@@ -28,7 +28,9 @@ enum OutMode : int {
 struct TileGrid {
     int P, M, N, K;
     int bands, rows_per_band, mt_per_band, ntiles_n, num_tiles;
-    int slice_loop;   // 1: a tile covers all P slices (bands == 1, t = mt * ntiles_n + nt)
+    int slice_loop;   // 1: a tile covers all P slices (bands == 1, t = mt * ntiles_n + nt) in one
+                      //    fp32 chain; 2 (CTA-pair kernel): the same tiles, each slice's partial
+                      //    summed in the band reducer's order
 };
 
 struct GemmOut {

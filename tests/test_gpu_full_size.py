@@ -127,3 +127,26 @@ def test_fused_mx_full_size(g):
         assert torch.isfinite(out.float()).all()
     finally:
         ctx.close()
+
+
+def test_onchip_full_size_bit_equal_to_pair_band_path(g, headline):
+    """GEMMAR_FUSE_ONCHIP at the headline shape: sampled rows against the oracle,
+    and the whole output bit-equal to the band path of the CTA-pair kernel."""
+    M = MMAX
+    ctx2 = g.gemmar_create(0, M, N, K, P, flags=g.GEMMAR_CTA_PAIR)
+    try:
+        outs = []
+        for flags in (g.GEMMAR_FUSE_ONCHIP, 0):
+            out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            g.fused_gemm_reduce(ctx2, headline["dA"], headline["dsa"], headline["dB"], headline["dsb"], out,
+                                bands=P, flags=flags)
+            torch.cuda.synchronize()
+            assert g.gemmar_status(ctx2)[0] == 0
+            outs.append(out)
+        assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+        rows = sample_rows(M, P, seed=11)
+        got = outs[0][torch.from_numpy(rows).cuda()].float().cpu().numpy()
+        ref, _ = oracle_rows(headline, M, rows)
+        check_bf16_output(got, ref, f"on-chip P=8 M={M}")
+    finally:
+        ctx2.close()

@@ -231,3 +231,40 @@ def test_pair_slice_loop(g, ctx_pair, P, M, N, K):
     ref, _ = oracle.gemm_reduce(A, sa, B, sb, 0)
     out = run_fused(g, ctx_pair, A, sa, B, sb, 0, P, flags=g.GEMMAR_FUSE_SLICES | g.GEMMAR_DEBUG_CANARY)
     check_bf16_output(out.float().cpu().numpy(), ref, f"pair slice loop P={P} M={M} N={N} K={K}")
+
+
+# ------------------------------------------------------------ partials summed on chip
+
+@pytest.mark.parametrize("P,M,N,K,bands", [(2, 256, 512, 256, 2), (3, 600, 768, 384, 3), (8, 1024, 256, 128, 8),
+                                           (1, 384, 512, 256, 1), (4, 520, 1024, 256, 4), (4, 512, 512, 256, 1)])
+def test_onchip_equals_band_path_bitwise(g, ctx_pair, P, M, N, K, bands):
+    A, sa, B, sb = blockscale_operands(P, M, N, K, seed=41 + P * M)
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, 0)
+    onchip = run_fused(g, ctx_pair, A, sa, B, sb, 0, bands, flags=g.GEMMAR_FUSE_ONCHIP | g.GEMMAR_DEBUG_CANARY)
+    band = run_fused(g, ctx_pair, A, sa, B, sb, 0, bands, flags=g.GEMMAR_DEBUG_CANARY)
+    check_bf16_output(onchip.float().cpu().numpy(), ref, f"on-chip P={P} M={M} N={N} K={K}")
+    # same per-slice fp32 partials, same summation order, one bf16 rounding
+    assert torch.equal(onchip.view(torch.int16), band.view(torch.int16))
+    again = run_fused(g, ctx_pair, A, sa, B, sb, 0, bands, flags=g.GEMMAR_FUSE_ONCHIP)
+    assert torch.equal(onchip.view(torch.int16), again.view(torch.int16))
+
+
+@pytest.mark.parametrize("kind,P,M,N,K", [(0, 2, 256, 384, 256), (1, 2, 256, 448, 256)])
+def test_onchip_falls_back_to_band_path(g, ctx, kind, P, M, N, K):
+    # shapes the on-chip path does not take (N % 256 != 0, mx scales): the band path runs
+    ops = blockscale_operands(P, M, N, K, seed=43 + P) if kind == 0 else mx_operands(P, M, N, K, seed=43 + P)
+    A, sa, B, sb = ops
+    a = run_fused(g, ctx, A, sa, B, sb, kind, P, flags=g.GEMMAR_FUSE_ONCHIP)
+    b = run_fused(g, ctx, A, sa, B, sb, kind, P)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_onchip_on_default_context_matches_one_cta_band_path(g, ctx):
+    P, M, N, K = 4, 512, 768, 256
+    A, sa, B, sb = blockscale_operands(P, M, N, K, seed=47)
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, 0)
+    onchip = run_fused(g, ctx, A, sa, B, sb, 0, P, flags=g.GEMMAR_FUSE_ONCHIP)
+    band = run_fused(g, ctx, A, sa, B, sb, 0, P)
+    check_bf16_output(onchip.float().cpu().numpy(), ref, "on-chip, default context")
+    d = (onchip.view(torch.int16).int() - band.view(torch.int16).int()).abs()
+    assert int(d.max()) <= 1
