@@ -14,16 +14,26 @@ template <int BN>
 __device__ __forceinline__ TileCoord decode_tile(int t, const TileGrid &g)
 {
     TileCoord c;
-    const int nt = t % g.ntiles_n;
-    int r = t / g.ntiles_n;
     if (g.slice_loop) {
+        // A tile reads all P slices' operands.  Tiles go in groups of 16 row
+        // tiles, column-major inside a group, so that the CTAs running at one
+        // time share A rows and B columns (about 16 x 9 tiles on 152 SMs) and
+        // each K-step's operands come from L2 more often than from HBM.
+        constexpr int kGroupM = 16;
+        const int mt_total = (g.M + 127) / 128;
+        const int per_group = kGroupM * g.ntiles_n;
+        const int m_first = (t / per_group) * kGroupM;
+        const int idx = t % per_group;
+        const int gm = min(kGroupM, mt_total - m_first);
         c.p = 0;
         c.b = 0;
-        c.m0 = r * 128;
-        c.n0 = nt * BN;
+        c.m0 = (m_first + idx % gm) * 128;
+        c.n0 = (idx / gm) * BN;
         c.valid_rows = min(128, g.M - c.m0);
         return c;
     }
+    const int nt = t % g.ntiles_n;
+    int r = t / g.ntiles_n;
     const int mt = r % g.mt_per_band;
     r /= g.mt_per_band;
     c.p = r % g.P;

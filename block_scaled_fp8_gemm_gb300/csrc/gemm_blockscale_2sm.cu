@@ -51,6 +51,7 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr int kRegsLow = 56;
 constexpr int kRegsHigh = 224;
 constexpr uint32_t kAbortGraceNs = 200000;   // let in-flight copies land before an aborting CTA exits
+constexpr int kGroupM = 8;                   // pair-rows per tile group in the slice loops
 
 struct PairTile {
     int b, p, m0, n0, band_end;
@@ -59,16 +60,26 @@ struct PairTile {
 __device__ __forceinline__ PairTile decode_pair(int t, const TileGrid &g)
 {
     PairTile c;
-    const int nt = t % g.ntiles_n;
-    int r = t / g.ntiles_n;
-    c.n0 = nt * 256;
     if (g.slice_loop) {
+        // A tile reads all P slices' operands.  Tiles go in groups of kGroupM
+        // pair-rows, column-major inside a group, so that the clusters running at
+        // one time share A rows and B columns (about 8 x 9 tiles on 76 clusters)
+        // and each K-step's operands come from L2 more often than from HBM.
+        const int mt2_total = (g.M + 255) / 256;
+        const int per_group = kGroupM * g.ntiles_n;
+        const int m_first = (t / per_group) * kGroupM;
+        const int idx = t % per_group;
+        const int gm = min(kGroupM, mt2_total - m_first);
         c.b = 0;
         c.p = 0;
-        c.m0 = r * 256;
+        c.n0 = (idx / gm) * 256;
+        c.m0 = (m_first + idx % gm) * 256;
         c.band_end = g.M;
         return c;
     }
+    const int nt = t % g.ntiles_n;
+    int r = t / g.ntiles_n;
+    c.n0 = nt * 256;
     const int mt2_per_band = (g.rows_per_band + 255) / 256;
     const int mt2 = r % mt2_per_band;
     r /= mt2_per_band;
