@@ -41,6 +41,29 @@ def flops(P, M, N, K):
     return 2.0 * P * M * N * K
 
 
+# ------------------------------------------------------------------ ranks
+# N > 1 runs N independent replicas of the layer (one process per GPU, no data
+# exchange between them); the job's time is the slowest rank's and its work is
+# the sum of the ranks'.
+
+def max_over_ranks(x, device="cpu"):
+    """The largest value of x over the ranks of the default process group
+    (x itself when there is none or it has one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_tflops(world, flop_per_replica, ms):
+    """Whole-job TFLOP/s of `world` replicas that each did flop_per_replica
+    within the slowest rank's ms."""
+    return world * flop_per_replica / (ms * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -302,10 +325,7 @@ def run_ours(args, rank, world, local_rank):
     code, detail = g.gemmar_status(ctx)
     if code != 0:
         raise RuntimeError(f"device status {g.STATUS_NAMES.get(code)} at site {detail}")
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
 
     fl = flops(P, M, N, K)
     gemm_ms = phases["gemm"] / max(ncalls, 1)
@@ -442,10 +462,7 @@ def run_ours(args, rank, world, local_rank):
     t1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = t0.elapsed_time(t1) / n_e2e
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
     code, detail = g.gemmar_status(ctx)
     if code != 0:
         raise RuntimeError(f"device status {g.STATUS_NAMES.get(code)} at site {detail}")
@@ -457,7 +474,7 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0:
         line = {
             "metric": METRIC,
-            "value": world * fl / (ms * 1e-3) / 1e12,
+            "value": replica_tflops(world, fl, ms),
             "unit": "TFLOP/s",
             "n_gpus": world,
             "steps": args.steps,
@@ -483,7 +500,7 @@ def run_ours(args, rank, world, local_rank):
             "band_reduce": {"us": reduce_ms * 1e3, "GB/s": reduce_gbs, "bytes": reduce_bytes,
                             "frac_of_measured_hbm": reduce_gbs / peaks["hbm_gbs"]},
             **extra,
-            "e2e": {"value": world * fl / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "e2e": {"value": replica_tflops(world, fl, e2e_ms), "unit": "TFLOP/s",
                     "us_per_layer": e2e_ms * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": n_e2e,
                     "what": "per step: activations (A codes + 1x128 scales) host->device, fused_gemm_reduce, "
