@@ -69,10 +69,10 @@ template <int UNITS>
 __device__ __forceinline__ void store_chunk(uint32_t stage, const uint4 (&v)[UNITS], char *gdst,
                                             int64_t row_stride_bytes, int rows_valid)
 {
-    static_assert(UNITS == 8 || UNITS == 4, "chunk is 128 or 64 bytes per row");
+    static_assert(UNITS == 8 || UNITS == 4 || UNITS == 2, "chunk is 128, 64 or 32 bytes per row");
     constexpr int ROWB = UNITS * 16;
     const int lane = threadIdx.x & 31;
-    const int sw = (UNITS == 8) ? (lane & 7) : ((lane >> 1) & 3);
+    const int sw = (UNITS == 8) ? (lane & 7) : (UNITS == 4) ? ((lane >> 1) & 3) : ((lane >> 2) & 1);
 #pragma unroll
     for (int u = 0; u < UNITS; ++u)
         ptx::st_shared_v4(stage + lane * ROWB + ((u ^ sw) * 16), v[u]);
@@ -82,7 +82,7 @@ __device__ __forceinline__ void store_chunk(uint32_t stage, const uint4 (&v)[UNI
     for (int i = 0; i < UNITS; ++i) {
         const int r = i * RPI + lane / UNITS;
         const int u = lane % UNITS;
-        const int rsw = (UNITS == 8) ? (r & 7) : ((r >> 1) & 3);
+        const int rsw = (UNITS == 8) ? (r & 7) : (UNITS == 4) ? ((r >> 1) & 3) : ((r >> 2) & 1);
         const uint4 val = ptx::ld_shared_v4(stage + r * ROWB + ((u ^ rsw) * 16));
         if (r < rows_valid)
             *reinterpret_cast<uint4 *>(gdst + r * row_stride_bytes + u * 16) = val;

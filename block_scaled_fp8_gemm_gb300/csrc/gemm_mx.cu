@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
     const TileGrid &g = prm.g;
     const int KB = g.K / 128;
     const int NKS = (g.slice_loop ? g.P : 1) * KB;   // K-blocks per tile
+    const bool exact = g.slice_loop == 2;            // slice partials summed on chip
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -150,37 +151,46 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
             uint32_t ph = 0, titer = 0;
             bool ok = true;
             const uint32_t sfa_t = tmem_base + kSfaCol, sfb_t = tmem_base + kSfbCol;
+            // An accumulation unit is a tile (band path, one-chain slice loop) or,
+            // with the partials summed on chip, one slice of a tile: each unit
+            // accumulates its K-blocks from zero into one TMEM buffer.
+            const int units = exact ? g.P : 1;
+            const int ks_per_unit = exact ? KB : NKS;
             for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
-                const uint32_t buf = titer & 1, tph = (titer >> 1) & 1;
-                if (!mbar_wait(tempty + buf, tph ^ 1, abort_flag, prm.status, prm.timeout_ns,
-                               SITE_MMA_TMEM_EMPTY))
-                    break;
-                const uint32_t d = tmem_base + buf * BN;
-                for (int ks = 0; ks < NKS; ++ks) {
-                    if (!mbar_wait(full + stage, ph, abort_flag, prm.status, prm.timeout_ns, SITE_MMA_FULL)) {
+                for (int un = 0; un < units && ok; ++un) {
+                    const uint32_t buf = titer & 1, tph = (titer >> 1) & 1;
+                    if (!mbar_wait(tempty + buf, tph ^ 1, abort_flag, prm.status, prm.timeout_ns,
+                                   SITE_MMA_TMEM_EMPTY)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t sf = smem_u32(smem + C::kOffSf + stage * C::kSfBytes);
-                    tc_cp_32x128b_warpx4(sfa_t, smem_desc(sf, 0, 128, 0));
-                    tc_cp_32x128b_warpx4(sfb_t, smem_desc(sf + 512, 0, 128, 0));
-                    tc_cp_32x128b_warpx4(sfb_t + 4, smem_desc(sf + 1024, 0, 128, 0));
-                    const uint64_t ad = desc_kmajor_sw128(smem_u32(smem + C::kOffA + stage * C::kABytes));
-                    const uint64_t bd = desc_kmajor_sw128(smem_u32(smem + C::kOffB + stage * C::kBBytes));
+                    const uint32_t d = tmem_base + buf * BN;
+                    for (int ks = 0; ks < ks_per_unit; ++ks) {
+                        if (!mbar_wait(full + stage, ph, abort_flag, prm.status, prm.timeout_ns, SITE_MMA_FULL)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sf = smem_u32(smem + C::kOffSf + stage * C::kSfBytes);
+                        tc_cp_32x128b_warpx4(sfa_t, smem_desc(sf, 0, 128, 0));
+                        tc_cp_32x128b_warpx4(sfb_t, smem_desc(sf + 512, 0, 128, 0));
+                        tc_cp_32x128b_warpx4(sfb_t + 4, smem_desc(sf + 1024, 0, 128, 0));
+                        const uint64_t ad = desc_kmajor_sw128(smem_u32(smem + C::kOffA + stage * C::kABytes));
+                        const uint64_t bd = desc_kmajor_sw128(smem_u32(smem + C::kOffB + stage * C::kBBytes));
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_mxf8(d, ad + 2 * k, bd + 2 * k, idesc_mx_e4m3(128, BN, (uint32_t)k), sfa_t, sfb_t,
-                                 (ks > 0 || k > 0) ? 1u : 0u);
-                    tc_commit(empty + stage);
-                    if (ks == NKS - 1)
-                        tc_commit(tfull + buf);
-                    if (++stage == C::kStages) {
-                        stage = 0;
-                        ph ^= 1;
+                        for (int k = 0; k < 4; ++k)
+                            mma_mxf8(d, ad + 2 * k, bd + 2 * k, idesc_mx_e4m3(128, BN, (uint32_t)k), sfa_t, sfb_t,
+                                     (ks > 0 || k > 0) ? 1u : 0u);
+                        tc_commit(empty + stage);
+                        if (ks == ks_per_unit - 1)
+                            tc_commit(tfull + buf);
+                        if (++stage == C::kStages) {
+                            stage = 0;
+                            ph ^= 1;
+                        }
                     }
+                    ++titer;
                 }
-                ++titer;
             }
             tc_commit(final_bar);
             const uint64_t t0 = globaltimer();
@@ -200,7 +210,58 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         const uint32_t staging = smem_u32(smem + C::kOffStaging + ew * 4096);
         const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
         uint32_t titer = 0;
-        for (int t = blockIdx.x; t < g.num_tiles; t += gridDim.x) {
+        if (exact) {
+            // Each slice's fp32 partial arrives in a TMEM buffer of its own; the
+            // warp folds its 16-column groups h, h+2, ... into a running sum in the
+            // band reducer's order (run = W_0, then run = run + W_p) and stores
+            // bf16(run) once per tile.
+            constexpr int NH = BN / 32;   // 16-column groups per warp
+            bool ok = true;
+            for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
+                const TileCoord tc = decode_tile<BN>(t, g);
+                float run[NH * 16];
+                for (int sl = 0; sl < g.P; ++sl) {
+                    const uint32_t buf = titer & 1, tph = (titer >> 1) & 1;
+                    if (!mbar_wait(tfull + buf, tph, abort_flag, prm.status, prm.timeout_ns, SITE_EPI_TMEM_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int i = 0; i < NH; ++i) {
+                        uint32_t r[16];
+                        tmem_ld_x16(lane_base + buf * BN + (h + 2 * i) * 16, r);
+                        tmem_wait_ld(r);
+                        if (i == NH - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0)
+                                mbar_arrive(tempty + buf);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            run[i * 16 + j] = sl == 0 ? __uint_as_float(r[j]) : __fadd_rn(run[i * 16 + j], __uint_as_float(r[j]));
+                    }
+                    ++titer;
+                }
+                if (!ok)
+                    break;
+                const int rows_valid = max(0, min(32, tc.valid_rows - q * 32));
+                char *base = tile_out_base(prm.o, g, tc, 2) + (int64_t)q * 32 * g.N * 2;
+#pragma unroll
+                for (int i = 0; i < NH; ++i) {
+                    uint4 v[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float *a = &run[i * 16 + u * 8];
+                        v[u] = make_uint4(bf16x2_from_f32(a[0], a[1]), bf16x2_from_f32(a[2], a[3]),
+                                          bf16x2_from_f32(a[4], a[5]), bf16x2_from_f32(a[6], a[7]));
+                    }
+                    store_chunk<2>(staging, v, base + (h + 2 * i) * 32, (int64_t)g.N * 2, rows_valid);
+                }
+            }
+        }
+        for (int t = blockIdx.x; t < g.num_tiles && !exact; t += gridDim.x) {
             const TileCoord tc = decode_tile<BN>(t, g);
             const uint32_t buf = titer & 1, tph = (titer >> 1) & 1;
             if (!mbar_wait(tfull + buf, tph, abort_flag, prm.status, prm.timeout_ns, SITE_EPI_TMEM_FULL))

@@ -414,10 +414,10 @@ GEMMAR_API int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A
     }
     if (!aligned16(out))
         return GEMMAR_ERR_ALIGN;
-    // on-chip partial sums: blockscale on the CTA-pair kernel; elsewhere the band path,
-    // whose bits it reproduces
-    const bool onchip = (flags & GEMMAR_FUSE_ONCHIP) && scale_kind == GEMMAR_SCALE_BLOCK128 &&
-                        plan_blockscale(P, M, N, K, bands, 2, ctx->num_sms, 1).pair;
+    // on-chip partial sums: mx on the mx kernel, blockscale on the CTA-pair kernel
+    // (N % 256 == 0); other blockscale shapes take the band path, whose bits they reproduce
+    const bool onchip = (flags & GEMMAR_FUSE_ONCHIP) &&
+                        (scale_kind == GEMMAR_SCALE_MX32 || plan_blockscale(P, M, N, K, bands, 2, ctx->num_sms, 1).pair);
     const bool slices = onchip || ((flags & GEMMAR_FUSE_SLICES) != 0 && !(flags & GEMMAR_FUSE_ONCHIP));
     if (!slices && blocked_partial_floats(P, M, bands, N) > ctx->W_floats)
         return GEMMAR_ERR_WORKSPACE;

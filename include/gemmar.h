@@ -88,7 +88,8 @@ enum { GEMMAR_SCALE_BLOCK128 = 0, GEMMAR_SCALE_MX32 = 1 };
                                              partials, no band reduce); see fused_gemm_reduce */
 #define GEMMAR_FUSE_ONCHIP     (1u << 6)  /* fused: the P slice partials of a tile stay on chip and are
                                              summed in the band reducer's order; bit-equal to the band
-                                             path of a GEMMAR_CTA_PAIR context; see fused_gemm_reduce */
+                                             path (blockscale: of a GEMMAR_CTA_PAIR context); see
+                                             fused_gemm_reduce */
 
 /* Largest number of K-slices ("ranks") one call takes. */
 #define GEMMAR_MAX_P 8
@@ -261,15 +262,16 @@ int quant_mx_e4m3(gemmar_ctx *ctx, const float *x, int64_t R, int64_t C, uint8_t
  * the band path's, so the two are not bit-equal.  bands is then ignored
  * (it must still satisfy the shape rules).
  *
- * With GEMMAR_FUSE_ONCHIP (blockscale, N % 256 == 0, a GPU that runs CTA
- * pairs) each 256 x 256 output tile computes the P slice partials one after
- * another, each exactly as the band path computes it (fp32, its own K-blocks
- * from zero), and sums them in the band reducer's order, ((W_0 + W_1) + W_2)
- * + ..., in fp32, the running sum held in shared memory, before the single
- * bf16 rounding.  The output is bit-equal to the band path run on the
- * CTA-pair kernel (a GEMMAR_CTA_PAIR context) for any bands, without the
- * 2 x P*M*N*4 bytes of partial traffic.  Other shapes and the mx scale kind
- * take the band path.  Takes precedence over GEMMAR_FUSE_SLICES.
+ * With GEMMAR_FUSE_ONCHIP each output tile computes the P slice partials one
+ * after another, each exactly as the band path computes it (fp32, its own
+ * K-blocks from zero), and sums them in the band reducer's order, ((W_0 +
+ * W_1) + W_2) + ..., in fp32 before the single bf16 rounding, without the
+ * 2 x P*M*N*4 bytes of partial traffic.  Blockscale (N % 256 == 0, a GPU that
+ * runs CTA pairs) runs on the CTA-pair kernel, the running sum in shared
+ * memory: bit-equal to the band path of a GEMMAR_CTA_PAIR context.  mx runs on
+ * the mx kernel, each slice accumulating in a TMEM buffer of its own and the
+ * running sum in registers: bit-equal to the mx band path.  Other blockscale
+ * shapes take the band path.  Takes precedence over GEMMAR_FUSE_SLICES.
  */
 int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A, const void *const *sa,
                       const uint8_t *const *B, const void *const *sb, int scale_kind,

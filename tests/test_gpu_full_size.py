@@ -125,6 +125,14 @@ def test_fused_mx_full_size(g):
         ref, _ = oracle.gemm_reduce(A, ea, B, eb, 1, rows=rows)
         check_bf16_output(got, ref, f"fused mx P=4 M={M} N={N} K={K}")
         assert torch.isfinite(out.float()).all()
+        # the slices summed on chip reproduce the band path's bits
+        onchip = torch.empty_like(out)
+        g.fused_gemm_reduce(ctx, [dev(a) for a in A], [dev(s) for s in ea], [dev(b) for b in B],
+                            [dev(s) for s in eb], onchip, scale_kind=g.GEMMAR_SCALE_MX32, bands=Pm,
+                            flags=g.GEMMAR_FUSE_ONCHIP)
+        torch.cuda.synchronize()
+        assert g.gemmar_status(ctx)[0] == 0
+        assert torch.equal(onchip.view(torch.int16), out.view(torch.int16))
     finally:
         ctx.close()
 

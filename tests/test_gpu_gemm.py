@@ -249,13 +249,17 @@ def test_onchip_equals_band_path_bitwise(g, ctx_pair, P, M, N, K, bands):
     assert torch.equal(onchip.view(torch.int16), again.view(torch.int16))
 
 
-@pytest.mark.parametrize("kind,P,M,N,K", [(0, 2, 256, 384, 256), (1, 2, 256, 448, 256)])
-def test_onchip_falls_back_to_band_path(g, ctx, kind, P, M, N, K):
-    # shapes the on-chip path does not take (N % 256 != 0, mx scales): the band path runs
+@pytest.mark.parametrize("kind,P,M,N,K", [(0, 2, 256, 384, 256), (1, 2, 256, 448, 256), (1, 3, 600, 384, 256),
+                                          (1, 4, 384, 256, 128), (1, 1, 256, 448, 256), (1, 8, 512, 448, 128)])
+def test_onchip_equals_band_path_default_context(g, ctx, kind, P, M, N, K):
+    # blockscale with N % 256 != 0 takes the band path; mx sums its slices on chip
+    # (a TMEM buffer per slice, the running sum in registers): bit-equal either way
     ops = blockscale_operands(P, M, N, K, seed=43 + P) if kind == 0 else mx_operands(P, M, N, K, seed=43 + P)
     A, sa, B, sb = ops
-    a = run_fused(g, ctx, A, sa, B, sb, kind, P, flags=g.GEMMAR_FUSE_ONCHIP)
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, kind)
+    a = run_fused(g, ctx, A, sa, B, sb, kind, P, flags=g.GEMMAR_FUSE_ONCHIP | g.GEMMAR_DEBUG_CANARY)
     b = run_fused(g, ctx, A, sa, B, sb, kind, P)
+    check_bf16_output(a.float().cpu().numpy(), ref, f"on-chip kind={kind} P={P} M={M} N={N} K={K}")
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
