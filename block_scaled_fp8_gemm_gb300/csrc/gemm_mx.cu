@@ -15,6 +15,10 @@
 //              serves every stage.
 //   warps 4-11 epilogue: drain the tile's fp32 accumulator (double-buffered
 //              across tiles) in 32-column chunks and store it.
+// With the slice partials summed on chip (TileGrid::slice_loop == 2) every
+// slice of a tile accumulates from zero in its own TMEM buffer -- exactly the
+// band path's partial -- and the epilogue folds it into a register running sum
+// in the band reducer's order while the MMA fills the other buffer.
 // TMEM: accumulators at columns [0, 2*BN), A scales at 480..483, B scales at
 // 488..495.
 #include "epilogue.cuh"

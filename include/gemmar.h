@@ -80,10 +80,11 @@ enum { GEMMAR_SCALE_BLOCK128 = 0, GEMMAR_SCALE_MX32 = 1 };
 #define GEMMAR_FAULT_SKIP_BAND (1u << 2)  /* fused, testing only: band 0 is never signalled, so the
                                              reducer's bounded wait expires (GEMMAR_ERR_TIMEOUT) */
 #define GEMMAR_NO_SELF_TEST    (1u << 3)  /* create: skip the closed-form self-test */
-#define GEMMAR_CTA_PAIR        (1u << 5)  /* create: run blockscale GEMMs on the CTA-pair kernel (256 x 128
-                                             tiles over two SMs, partials streamed from registers) instead
-                                             of the one-CTA kernel; same results within tolerance, slower
-                                             on the wo_b shapes, kept for comparison */
+#define GEMMAR_CTA_PAIR        (1u << 5)  /* create: run blockscale GEMMs with N % 256 == 0 on the CTA-pair
+                                             kernel (256 x 256 tiles over two SMs, band partials parked in
+                                             shared memory and sent by bulk async copies) instead of the
+                                             one-CTA kernel; same results within tolerance; on the wo_b
+                                             band path about as fast */
 #define GEMMAR_FUSE_SLICES     (1u << 4)  /* fused: each output tile accumulates all P slices itself (no
                                              partials, no band reduce); see fused_gemm_reduce */
 #define GEMMAR_FUSE_ONCHIP     (1u << 6)  /* fused: the P slice partials of a tile stay on chip and are

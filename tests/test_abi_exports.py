@@ -64,3 +64,39 @@ def test_shape_rules_host_only(lib):
     assert sup(9, 128, 256, 128, 1, 0) == ARG           # more slices than the ABI takes
     assert sup(2, 128, 256, 128, 0, 0) == ARG
     assert sup(2, 128, 256, 128, 2, 7) == ARG           # unknown scale kind
+
+
+def declared_constants():
+    text = open(HEADER).read()
+    consts = {}
+    for body in re.findall(r"enum\s*\{(.*?)\}", re.sub(r"/\*.*?\*/", "", text, flags=re.S), flags=re.S):
+        for name, value in re.findall(r"(GEMMAR_[A-Z0-9_]+)\s*=\s*(\d+)", body):
+            consts[name] = int(value)
+    for name, expr in re.findall(r"^#define\s+(GEMMAR_[A-Z0-9_]+)\s+([^/\n]+)", text, flags=re.M):
+        expr = expr.strip()
+        m = re.fullmatch(r"\(\s*1u?\s*<<\s*(\d+)\s*\)", expr)
+        if m:
+            consts[name] = 1 << int(m.group(1))
+            continue
+        expr = expr.replace("u", "") if re.fullmatch(r"[\d\s\*\(\)u]+", expr) else expr
+        try:
+            consts[name] = int(eval(expr, {"__builtins__": {}}))
+        except Exception:
+            pass
+    return consts
+
+
+def test_binding_constants_match_the_header(lib):
+    import block_scaled_fp8_gemm_gb300 as g
+    consts = declared_constants()
+    for required in ("GEMMAR_FP8_WIRE", "GEMMAR_FUSE_SLICES", "GEMMAR_FUSE_ONCHIP", "GEMMAR_CTA_PAIR",
+                     "GEMMAR_SCALE_BLOCK128", "GEMMAR_SCALE_MX32"):
+        assert required in consts, required
+    for name, value in consts.items():
+        if hasattr(g, name):
+            assert getattr(g, name) == value, (name, getattr(g, name), value)
+    # every flag bit is distinct
+    flags = [v for n, v in consts.items() if n in ("GEMMAR_FP8_WIRE", "GEMMAR_DEBUG_CANARY", "GEMMAR_FAULT_SKIP_BAND",
+                                                   "GEMMAR_NO_SELF_TEST", "GEMMAR_FUSE_SLICES", "GEMMAR_CTA_PAIR",
+                                                   "GEMMAR_FUSE_ONCHIP")]
+    assert len(flags) == len(set(flags)) == 7
