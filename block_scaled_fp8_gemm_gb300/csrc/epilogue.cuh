@@ -120,17 +120,41 @@ __device__ __forceinline__ void store_partial_chunk(float4 *tile_base, int q, in
         __stcg(dst + u * 32, make_float4(v[u * 4 + 0], v[u * 4 + 1], v[u * 4 + 2], v[u * 4 + 3]));
 }
 
-// Publish one retired tile (per warp) to the band reducer: the warp barrier
-// orders every lane's stores before lane 0, whose gpu-scope fence and release
-// add then make them visible to the reducer's acquire.
-__device__ __forceinline__ void signal_band(const GemmOut &o, int band)
+// Publish n retired tiles (per warp) of one band to the band reducer: the
+// warp barrier orders every lane's stores before lane 0, whose gpu-scope fence
+// and release add then make them visible to the reducer's acquire.
+__device__ __forceinline__ void signal_band(const GemmOut &o, int band, uint32_t n = 1u)
 {
     __syncwarp();
     if ((threadIdx.x & 31) == 0 && band != o.skip_band) {
         __threadfence();
-        ptx::red_release_add(o.band_done + band, 1u);
+        ptx::red_release_add(o.band_done + band, n);
     }
 }
+
+// A warp's band signals, batched per run of same-band tiles: the fence in
+// signal_band waits until every partial store the warp has in flight is
+// performed (about a microsecond after a tile's 128 KB), so a warp counts the
+// tiles it retires and publishes a band's count once, when its next tile
+// belongs to another band, or at the end.  The counts the reducer waits for
+// are unchanged.  Whole warp must call.
+struct BandSignals {
+    int band = -1;
+    uint32_t n = 0;
+    __device__ __forceinline__ void add(const GemmOut &o, int b)
+    {
+        if (b != band)
+            flush(o);
+        band = b;
+        ++n;
+    }
+    __device__ __forceinline__ void flush(const GemmOut &o)
+    {
+        if (n != 0)
+            signal_band(o, band, n);
+        n = 0;
+    }
+};
 
 template <int N>
 __device__ __forceinline__ void setmaxnreg_dec()

@@ -189,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
         uint32_t kiter = 0;
         bool ok = true;
         const int nsl = g.slice_loop ? g.P : 1;
+        BandSignals signals;
         for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
             const TileCoord tc = decode_tile<BN>(t, g);
             const int64_t mrow = min(tc.m0 + row, g.M - 1);
@@ -280,8 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
                 }
             }
             if (prm.o.out_mode == OUT_PARTIAL_F32)
-                signal_band(prm.o, tc.b);
+                signals.add(prm.o, tc.b);
         }
+        if (ok)
+            signals.flush(prm.o);
     }
 
     __syncwarp();

@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         const uint32_t staging = smem_u32(smem + C::kOffStaging + ew * 4096);
         const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
         uint32_t titer = 0;
+        BandSignals signals;
         if (exact) {
             // Each slice's fp32 partial arrives in a TMEM buffer of its own; the
             // warp folds its 16-column groups h, h+2, ... into a running sum in the
@@ -305,9 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                 }
             }
             if (prm.o.out_mode == OUT_PARTIAL_F32)
-                signal_band(prm.o, tc.b);
+                signals.add(prm.o, tc.b);
             ++titer;
         }
+        if (!exact)
+            signals.flush(prm.o);
     }
 
     __syncwarp();
