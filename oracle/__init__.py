@@ -131,13 +131,21 @@ def quant_mx(x: np.ndarray):
     return codes, sb
 
 
+def quant_ptpc(x: np.ndarray):
+    """ptpc quantiser: one fp32 scale per row over the whole row (per token for
+    A [M,K], per output channel for B [N,K]) -> (codes uint8, scales fp32 [R])."""
+    codes, scales = quant_block(x, 1, np.asarray(x).shape[1])
+    return codes, np.ascontiguousarray(scales[:, 0])
+
+
 # --- GEMM + reduction --------------------------------------------------------
 
 def gemm_reduce(A, sa, B, sb, scale_kind: int = 0, rows=None, want_ref: bool = True):
     """fp64 P-way sum of per-slice scaled GEMMs for the listed rows.
 
     A, sa, B, sb are lists of P numpy arrays (A_p [M,K] uint8, B_p [N,K] uint8;
-    sa/sb fp32 block scales for scale_kind 0, ue8m0 bytes for scale_kind 1).
+    sa/sb fp32 block scales for scale_kind 0, ue8m0 bytes for scale_kind 1,
+    fp32 per-row scales sa [M] and sb [N] for scale_kind 2, ptpc).
     Returns (ref fp64 [nrows,N] or None, out bf16 bits uint16 [nrows,N]).
     """
     P = len(A)

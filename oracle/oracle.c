@@ -339,12 +339,51 @@ void orc_gemm_mx_acc(const uint8_t *A, const uint8_t *ea, const uint8_t *B, cons
 }
 
 /*
+ * ptpc GEMM of one K-slice: one fp32 scale per row of A (per token) and one
+ * per row of B (per output channel), the quantisation mode the MORI benchmark
+ * runs by default ("A CK-shaped 4-wave GEMM" paragraph of "Negative results":
+ * `--quant ptpc`), read as per-token / per-channel:
+ *   G[m,n] = (sa[m] * sb[n]) * sum_k a[m,k] b[n,k]
+ * sa is [M], sb is [N].  Added into acc as above.
+ */
+void orc_gemm_ptpc_acc(const uint8_t *A, const float *sa, const uint8_t *B, const float *sb,
+                       int64_t M, int64_t N, int64_t K, const int64_t *rows, int64_t nrows,
+                       double *acc)
+{
+    if (rows == NULL) nrows = M;
+    double *bdec = (double *)malloc(sizeof(double) * (size_t)(N * K));
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < N * K; ++i)
+        bdec[i] = e4m3_value[B[i]];
+#pragma omp parallel
+    {
+        double *arow = (double *)malloc(sizeof(double) * (size_t)K);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < nrows; ++i) {
+            int64_t m = rows ? rows[i] : i;
+            for (int64_t k = 0; k < K; ++k)
+                arow[k] = e4m3_value[A[m * K + k]];
+            for (int64_t n = 0; n < N; ++n) {
+                const double *brow = bdec + n * K;
+                double dot = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    dot += arow[k] * brow[k];
+                acc[i * N + n] += ((double)sa[m] * (double)sb[n]) * dot;
+            }
+        }
+        free(arow);
+    }
+    free(bdec);
+}
+
+/*
  * The whole path for the listed rows: R = sum_{p=0}^{P-1} G_p in fp64, then
  * out = bf16_rn(R) ([PR40757] "What": a block-scale fp8 GEMM followed by the
  * all-reduce of the [M, hidden] result; [MORI] "The fp8 wire": the reduce
  * accumulates in fp32 and the output is bf16 -- here the sum is carried in
  * fp64 and rounded once, the plain definition the fp32 sum approximates).
- * scale_kind 0 = block 128 (sa/sb fp32), 1 = mx 32 (sa/sb ue8m0 bytes).
+ * scale_kind 0 = block 128 (sa/sb fp32), 1 = mx 32 (sa/sb ue8m0 bytes),
+ * 2 = ptpc (sa [M], sb [N] fp32).
  * ref (optional, [nrows,N] fp64) receives R; out receives bf16 bits.
  */
 void orc_gemm_reduce(int P, const uint8_t *const *A, const void *const *sa,
@@ -359,9 +398,12 @@ void orc_gemm_reduce(int P, const uint8_t *const *A, const void *const *sa,
         if (scale_kind == 0)
             orc_gemm_blockscale_acc(A[p], (const float *)sa[p], B[p], (const float *)sb[p],
                                     M, N, K, rows, nrows, acc);
-        else
+        else if (scale_kind == 1)
             orc_gemm_mx_acc(A[p], (const uint8_t *)sa[p], B[p], (const uint8_t *)sb[p],
                             M, N, K, rows, nrows, acc);
+        else
+            orc_gemm_ptpc_acc(A[p], (const float *)sa[p], B[p], (const float *)sb[p],
+                              M, N, K, rows, nrows, acc);
     }
     if (out)
         for (int64_t i = 0; i < nrows * N; ++i)

@@ -179,3 +179,71 @@ def test_reduce_f32_ordered_matches_numpy_and_library():
     # P = 1 is the identity up to the bf16 rounding
     assert np.array_equal(oracle.reduce_f32_ordered(W[:1]),
                           torch.from_numpy(W[0]).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+
+
+# ------------------------------------------------------------------ ptpc (scale_kind 2)
+
+def make_ptpc(P, M, N, K, seed=0):
+    A, sa, B, sb = [], [], [], []
+    for p in range(P):
+        a, s = oracle.quant_ptpc(synthetic.normal(seed, synthetic.TID_A, p, (M, K)))
+        b, t = oracle.quant_ptpc(synthetic.normal(seed, synthetic.TID_B, p, (N, K), sigma=0.02))
+        A.append(a); sa.append(s); B.append(b); sb.append(t)
+    return A, sa, B, sb
+
+
+def test_ptpc_quantiser_is_the_row_codec():
+    # per-token / per-channel scales are one group per row: the fp8-wire row codec
+    x = synthetic.normal(3, synthetic.TID_X, 0, (40, 384))
+    q1, s1 = oracle.quant_ptpc(x)
+    q2, s2 = oracle.rowquant(x)
+    assert np.array_equal(q1, q2) and np.array_equal(s1, s2)
+
+
+def test_p1_equals_plain_matmul_ptpc():
+    A, sa, B, sb = make_ptpc(1, 72, 200, 384, seed=21)
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, 2)
+    a = TABLE[A[0]] * sa[0].astype(np.float64)[:, None]
+    b = TABLE[B[0]] * sb[0].astype(np.float64)[:, None]
+    plain = a @ b.T
+    assert np.max(np.abs(ref - plain)) <= 1e-12 * np.max(np.abs(plain))
+
+
+def test_ptpc_with_unit_scales_equals_blockscale_with_unit_scales():
+    # the two scale kinds agree where they describe the same operands
+    A, _, B, _ = make_ptpc(2, 16, 256, 256, seed=22)
+    one_a = [np.ones((16,), np.float32)] * 2
+    one_b = [np.ones((256,), np.float32)] * 2
+    r_pt, o_pt = oracle.gemm_reduce(A, one_a, B, one_b, 2)
+    r_bs, o_bs = oracle.gemm_reduce(A, [np.ones((16, 2), np.float32)] * 2, B, [np.ones((2, 2), np.float32)] * 2, 0)
+    assert np.max(np.abs(r_pt - r_bs)) <= 1e-13 * np.max(np.abs(r_bs))
+
+
+def test_ptpc_scale_invariances_and_zero_rows():
+    A, sa, B, sb = make_ptpc(2, 24, 256, 256, seed=23)
+    ref, out = oracle.gemm_reduce(A, sa, B, sb, 2)
+    ref2, out2 = oracle.gemm_reduce(A, [s * np.float32(4.0) for s in sa], B, [s / np.float32(4.0) for s in sb], 2)
+    assert np.array_equal(ref, ref2) and np.array_equal(out, out2)
+    sa0 = [s.copy() for s in sa]
+    sb0 = [s.copy() for s in sb]
+    for p in range(2):
+        sa0[p][5] = 0.0                    # token 5 scaled to zero in every slice
+        sb0[p][200] = 0.0                  # channel 200 scaled to zero in every slice
+    r3, o3 = oracle.gemm_reduce(A, sa0, B, sb0, 2)
+    assert np.all(r3[5] == 0) and np.all(o3[5] == 0)
+    assert np.all(r3[:, 200] == 0) and np.all(o3[:, 200] == 0)
+
+
+def test_bruteforce_ptpc_exact_rational():
+    A, sa, B, sb = make_ptpc(2, 6, 8, 128, seed=24)
+    ref, out = oracle.gemm_reduce(A, sa, B, sb, 2)
+    for m in range(6):
+        for n in range(8):
+            tot, mag = Fraction(0), Fraction(0)
+            for p in range(2):
+                dot = sum(Fraction(float(TABLE[A[p][m, k]])) * Fraction(float(TABLE[B[p][n, k]])) for k in range(128))
+                term = Fraction(float(sa[p][m])) * Fraction(float(sb[p][n])) * dot
+                tot += term
+                mag += abs(term)
+            assert out[m, n] == bf16_nearest_bruteforce(tot)
+            assert abs(Fraction(float(ref[m, n])) - tot) <= mag * Fraction(8, 2 ** 53)
