@@ -46,6 +46,7 @@ GEMMAR_DTYPE_F32 = 0
 GEMMAR_DTYPE_BF16 = 1
 GEMMAR_SCALE_BLOCK128 = 0
 GEMMAR_SCALE_MX32 = 1
+GEMMAR_SCALE_PTPC = 2
 GEMMAR_FP8_WIRE = 1 << 0
 GEMMAR_DEBUG_CANARY = 1 << 1
 GEMMAR_FAULT_SKIP_BAND = 1 << 2
@@ -73,6 +74,7 @@ _SIGS = {
     "gemmar_phase_times": (_I, [_P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_I)]),
     "gemm_blockscale_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P]),
     "gemm_mxfp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P]),
+    "gemm_ptpc_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P]),
     "band_reduce": (_I, [_P, _P, _I, _I64, _I64, _I, _P, _P]),
     "rowquant_e4m3": (_I, [_P, _P, _I, _I64, _I64, _P, _P, _P]),
     "rowdequant_e4m3": (_I, [_P, _P, _P, _I64, _I64, _P, _P]),
@@ -226,6 +228,15 @@ def gemm_blockscale_fp8(ctx: Context, A, sa, B, sb, C, stream=None) -> None:
     _check(_lib.gemm_blockscale_fp8(ctx.handle, _u8(A, "A"), _f32(sa, "sa"), _u8(B, "B"), _f32(sb, "sb"),
                                     _ptr(C, "C"), _cdtype(C), M, N, K, _stream(stream)),
            "gemm_blockscale_fp8")
+
+
+def gemm_ptpc_fp8(ctx: Context, A, sa, B, sb, C, stream=None) -> None:
+    """C = (sa[m]*sb[n]) * A @ B^T with per-token sa [M] and per-channel sb [N] (fp32)."""
+    M, K = A.shape
+    N = B.shape[0]
+    _check(_lib.gemm_ptpc_fp8(ctx.handle, _u8(A, "A"), _f32(sa, "sa"), _u8(B, "B"), _f32(sb, "sb"),
+                              _ptr(C, "C"), _cdtype(C), M, N, K, _stream(stream)),
+           "gemm_ptpc_fp8")
 
 
 def gemm_mxfp8(ctx: Context, A, ea, B, eb, C, stream=None) -> None:

@@ -31,12 +31,12 @@ namespace {
 constexpr uint32_t kSfaCol = 480;
 constexpr uint32_t kSfbCol = 488;
 
-template <int BN>
+template <int BN, bool PT>
 struct MxCfg {
-    static constexpr int kStages = (BN == 224) ? 4 : 5;
+    static constexpr int kStages = PT ? (BN == 256 ? 4 : 6) : (BN == 224 ? 4 : 5);
     static constexpr int kABytes = 128 * 128;
     static constexpr int kBBytes = BN * 128;
-    static constexpr int kSfBytes = 512 + 1024;
+    static constexpr int kSfBytes = PT ? 0 : 512 + 1024;
     static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
     static constexpr int kEpiWarps = 8;
     static constexpr int kStagingBytes = kEpiWarps * 4096;
@@ -51,15 +51,44 @@ struct MxCfg {
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kBBytes % 1024 == 0, "B tiles stay 1024-byte aligned");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
-    static_assert(2 * BN <= (int)kSfaCol, "accumulators below the scale columns");
+    static_assert(PT ? 2 * BN <= 512 : 2 * BN <= (int)kSfaCol, "accumulators below the scale columns");
 };
 
 constexpr int kThreads = 384;
+constexpr int kRegsLow = 56;    // warpgroup 0 (producer, MMA) after setmaxnreg.dec
+constexpr int kRegsHigh = 224;  // warpgroups 1-2 (epilogue) after setmaxnreg.inc
 
-template <int BN>
+// Four channel scales.  The load is ordered after the preceding TMEM wait (asm
+// volatile) so the compiler keeps it next to its use instead of hoisting every
+// group's scales to the top of the slice, which spills the running sum.
+__device__ __forceinline__ float4 ld_scales4(const float *p)
+{
+    float4 v;
+    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+// Scale one 16-column group of a ptpc tile row in place: w = (sa * sb[n]) * acc,
+// both products rounded to fp32 (the blockscale promotion's order).
+__device__ __forceinline__ void ptpc_scale16(uint32_t *r, float sa, const float *sb)
+{
+#pragma unroll
+    for (int j4 = 0; j4 < 4; ++j4) {
+        const float4 b = ld_scales4(sb + 4 * j4);
+        const float bs[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            r[j4 * 4 + j] = __float_as_uint(__fmul_rn(__fmul_rn(sa, bs[j]), __uint_as_float(r[j4 * 4 + j])));
+    }
+}
+
+template <int BN, bool PT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_constant__ MxParams prm)
 {
-    using C = MxCfg<BN>;
+    using C = MxCfg<BN, PT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
@@ -105,7 +134,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0) {
+    if (warp < 4) {
+        // producer and MMA warps give registers to the epilogue warpgroups
+        setmaxnreg_dec<kRegsLow>();
+      if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
             int stage = 0, issued = 0;
@@ -124,12 +156,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                         ok = false;
                         break;
                     }
-                    uint8_t *sf = smem + C::kOffSf + stage * C::kSfBytes;
                     mbar_arrive_expect_tx(full + stage, C::kStageBytes);
                     tma_load_2d(smem + C::kOffA + stage * C::kABytes, &prm.tmA[p], full + stage, kb * 128, tc.m0);
                     tma_load_2d(smem + C::kOffB + stage * C::kBBytes, &prm.tmB[p], full + stage, kb * 128, tc.n0);
-                    bulk_load(sf, prm.sfa + (a_img + kb) * 512, 512, full + stage);
-                    bulk_load(sf + 512, prm.sfb + (b_img + kb) * 1024, 1024, full + stage);
+                    if constexpr (!PT) {
+                        uint8_t *sf = smem + C::kOffSf + stage * C::kSfBytes;
+                        bulk_load(sf, prm.sfa + (a_img + kb) * 512, 512, full + stage);
+                        bulk_load(sf + 512, prm.sfb + (b_img + kb) * 1024, 1024, full + stage);
+                    }
                     ++issued;
                     if (++stage == C::kStages) {
                         stage = 0;
@@ -175,16 +209,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t sf = smem_u32(smem + C::kOffSf + stage * C::kSfBytes);
-                        tc_cp_32x128b_warpx4(sfa_t, smem_desc(sf, 0, 128, 0));
-                        tc_cp_32x128b_warpx4(sfb_t, smem_desc(sf + 512, 0, 128, 0));
-                        tc_cp_32x128b_warpx4(sfb_t + 4, smem_desc(sf + 1024, 0, 128, 0));
                         const uint64_t ad = desc_kmajor_sw128(smem_u32(smem + C::kOffA + stage * C::kABytes));
                         const uint64_t bd = desc_kmajor_sw128(smem_u32(smem + C::kOffB + stage * C::kBBytes));
+                        if constexpr (PT) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            mma_mxf8(d, ad + 2 * k, bd + 2 * k, idesc_mx_e4m3(128, BN, (uint32_t)k), sfa_t, sfb_t,
-                                     (ks > 0 || k > 0) ? 1u : 0u);
+                            for (int k = 0; k < 4; ++k)
+                                mma_f8(d, ad + 2 * k, bd + 2 * k, idesc_f8_e4m3(128, BN), (ks > 0 || k > 0) ? 1u : 0u);
+                        } else {
+                            const uint32_t sf = smem_u32(smem + C::kOffSf + stage * C::kSfBytes);
+                            tc_cp_32x128b_warpx4(sfa_t, smem_desc(sf, 0, 128, 0));
+                            tc_cp_32x128b_warpx4(sfb_t, smem_desc(sf + 512, 0, 128, 0));
+                            tc_cp_32x128b_warpx4(sfb_t + 4, smem_desc(sf + 1024, 0, 128, 0));
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                mma_mxf8(d, ad + 2 * k, bd + 2 * k, idesc_mx_e4m3(128, BN, (uint32_t)k), sfa_t, sfb_t,
+                                         (ks > 0 || k > 0) ? 1u : 0u);
+                        }
                         tc_commit(empty + stage);
                         if (ks == ks_per_unit - 1)
                             tc_commit(tfull + buf);
@@ -205,7 +245,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                 }
             }
         }
-    } else if (warp >= 4) {
+      }
+    } else {
+        setmaxnreg_inc<kRegsHigh>();
         // ---------------------------------------------------- epilogue
         constexpr int NCH = BN / 32;
         const int ew = warp - 4;
@@ -224,8 +266,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
             bool ok = true;
             for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
                 const TileCoord tc = decode_tile<BN>(t, g);
+                const int64_t mrow = min(tc.m0 + q * 32 + lane, g.M - 1);
                 float run[NH * 16];
                 for (int sl = 0; sl < g.P; ++sl) {
+                    const float sa_m = PT ? __ldg(prm.pa[sl] + mrow) : 0.0f;
+                    const float *sb_sl = PT ? prm.pb[sl] + tc.n0 + h * 16 : nullptr;
                     const uint32_t buf = titer & 1, tph = (titer >> 1) & 1;
                     if (!mbar_wait(tfull + buf, tph, abort_flag, prm.status, prm.timeout_ns, SITE_EPI_TMEM_FULL)) {
                         ok = false;
@@ -237,6 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                         uint32_t r[16];
                         tmem_ld_x16(lane_base + buf * BN + (h + 2 * i) * 16, r);
                         tmem_wait_ld(r);
+                        if constexpr (PT)
+                            ptpc_scale16(r, sa_m, sb_sl + i * 32);
                         if (i == NH - 1) {
                             tc_fence_before();
                             __syncwarp();
@@ -273,12 +320,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                 break;
             tc_fence_after();
             const int rows_valid = max(0, min(32, tc.valid_rows - q * 32));
+            const float sa_m = PT ? __ldg(prm.pa[tc.p] + min(tc.m0 + q * 32 + lane, g.M - 1)) : 0.0f;
             const int esz = prm.o.out_mode == OUT_BF16 ? 2 : 4;
             char *base = tile_out_base(prm.o, g, tc, esz) + (int64_t)q * 32 * g.N * esz;
             for (int c = h; c < NCH; c += 2) {
                 uint32_t r[32];
                 tmem_ld_x32(lane_base + buf * BN + c * 32, r);
                 tmem_wait_ld(r);
+                if constexpr (PT) {
+                    ptpc_scale16(r, sa_m, prm.pb[tc.p] + tc.n0 + c * 32);
+                    ptpc_scale16(r + 16, sa_m, prm.pb[tc.p] + tc.n0 + c * 32 + 16);
+                }
                 if (c + 2 >= NCH) {
                     tc_fence_before();
                     __syncwarp();
@@ -321,27 +373,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         tmem_dealloc(tmem_base, C::kTmemCols);
 }
 
-template <int BN>
+template <int BN, bool PT>
 cudaError_t launch_bn(const MxParams &p, int grid, cudaStream_t s)
 {
-    using C = MxCfg<BN>;
+    using C = MxCfg<BN, PT>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e =
-            cudaFuncSetAttribute(gemm_mx_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+            cudaFuncSetAttribute(gemm_mx_kernel<BN, PT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         if (e != cudaSuccess)
             return e;
         configured = true;
     }
-    gemm_mx_kernel<BN><<<grid, kThreads, C::kSmemBytes, s>>>(p);
+    gemm_mx_kernel<BN, PT><<<grid, kThreads, C::kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }
 
-template <int BN>
+template <int BN, bool PT>
 int regs_of()
 {
     cudaFuncAttributes a;
-    if (cudaFuncGetAttributes(&a, gemm_mx_kernel<BN>) != cudaSuccess)
+    if (cudaFuncGetAttributes(&a, gemm_mx_kernel<BN, PT>) != cudaSuccess)
         return -1;
     return a.numRegs;
 }
@@ -351,12 +403,23 @@ int regs_of()
 cudaError_t launch_gemm_mx(const MxParams &p, int bn, int grid, cudaStream_t s)
 {
     if (bn == 224)
-        return launch_bn<224>(p, grid, s);
+        return launch_bn<224, false>(p, grid, s);
     if (bn == 128)
-        return launch_bn<128>(p, grid, s);
+        return launch_bn<128, false>(p, grid, s);
     return cudaErrorInvalidValue;
 }
 
-int gemm_mx_num_regs(int bn) { return bn == 224 ? regs_of<224>() : regs_of<128>(); }
+cudaError_t launch_gemm_ptpc(const MxParams &p, int bn, int grid, cudaStream_t s)
+{
+    if (bn == 256)
+        return launch_bn<256, true>(p, grid, s);
+    if (bn == 128)
+        return launch_bn<128, true>(p, grid, s);
+    return cudaErrorInvalidValue;
+}
+
+int gemm_mx_num_regs(int bn) { return bn == 224 ? regs_of<224, false>() : regs_of<128, false>(); }
+
+int gemm_ptpc_num_regs(int bn) { return bn == 256 ? regs_of<256, true>() : regs_of<128, true>(); }
 
 }  // namespace gemmar

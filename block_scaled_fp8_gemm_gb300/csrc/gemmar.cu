@@ -124,8 +124,8 @@ int shape_rules(int P, int64_t M, int64_t N, int64_t K, int bands, int scale_kin
         return GEMMAR_ERR_ARG;
     if (bands > kMaxBands || bands > M || M % bands != 0)
         return GEMMAR_ERR_SHAPE;
-    // N is tiled by 256/128 (blockscale: also the B-scale block) or 224/128 (mx)
-    const bool n_ok = scale_kind == GEMMAR_SCALE_BLOCK128 ? (N % 128 == 0) : (N % 128 == 0 || N % 224 == 0);
+    // N is tiled by 256/128 (blockscale: also the B-scale block; ptpc) or 224/128 (mx)
+    const bool n_ok = scale_kind == GEMMAR_SCALE_MX32 ? (N % 128 == 0 || N % 224 == 0) : (N % 128 == 0);
     if (!n_ok || K % 128 != 0)
         return GEMMAR_ERR_SHAPE;
     if (N > 65536 || K > 65536 || M > (int64_t(1) << 24))
@@ -134,6 +134,12 @@ int shape_rules(int P, int64_t M, int64_t N, int64_t K, int bands, int scale_kin
 }
 
 int mx_tile_n(int64_t N) { return (N % 224 == 0) ? 224 : 128; }
+int ptpc_tile_n(int64_t N) { return (N % 256 == 0) ? 256 : 128; }
+
+bool known_scale_kind(int k)
+{
+    return k == GEMMAR_SCALE_BLOCK128 || k == GEMMAR_SCALE_MX32 || k == GEMMAR_SCALE_PTPC;
+}
 
 TileGrid make_grid(int P, int64_t M, int64_t N, int64_t K, int bands, int bn, int slice_loop = 0)
 {
@@ -204,10 +210,33 @@ int run_gemm(gemmar_ctx *ctx, int P, const uint8_t *const *A, const void *const 
         prm.status = ctx->status;
         prm.timeout_ns = ctx->timeout_ns;
         CUDA_OK(launch_blockscale(prm, pl, st));
+    } else if (scale_kind == GEMMAR_SCALE_PTPC) {
+        // one fp32 scale per row of A and of B: whole-K accumulation, scaled in the epilogue
+        const int bn = ptpc_tile_n(N);
+        if (slice_loop)
+            bands = 1;
+        if (gemm_ptpc_num_regs(bn) * 384 < 56 * 128 + 224 * 256)
+            return GEMMAR_ERR_DEVICE;
+        MxParams prm;
+        std::memset(&prm, 0, sizeof(prm));
+        for (int p = 0; p < P; ++p) {
+            if (!make_tmap_u8(&prm.tmA[p], A[p], M, K, 128) || !make_tmap_u8(&prm.tmB[p], B[p], N, K, bn))
+                return GEMMAR_ERR_CUDA;
+            prm.pa[p] = static_cast<const float *>(sa[p]);
+            prm.pb[p] = static_cast<const float *>(sb[p]);
+        }
+        prm.g = make_grid(P, M, N, K, bands, bn, slice_loop);
+        prm.o = o;
+        prm.status = ctx->status;
+        prm.timeout_ns = ctx->timeout_ns;
+        const int grid = std::min(prm.g.num_tiles, ctx->num_sms);
+        CUDA_OK(launch_gemm_ptpc(prm, bn, grid, st));
     } else {
         const int bn = mx_tile_n(N);
         if (slice_loop)
             bands = 1;
+        if (gemm_mx_num_regs(bn) * 384 < 56 * 128 + 224 * 256)
+            return GEMMAR_ERR_DEVICE;
         if (mx_sfa_bytes(P, M, K, bands) > ctx->sfa_bytes || mx_sfb_bytes(P, N, K, bn) > ctx->sfb_bytes)
             return GEMMAR_ERR_WORKSPACE;
         CUDA_OK(launch_mx_repack(reinterpret_cast<const uint8_t *const *>(sa),
@@ -252,7 +281,7 @@ int gemm_single(gemmar_ctx *ctx, const uint8_t *A, const void *sa, const uint8_t
 
 GEMMAR_API int gemmar_supports(int P, int64_t M, int64_t N, int64_t K, int bands, int scale_kind)
 {
-    if (scale_kind != GEMMAR_SCALE_BLOCK128 && scale_kind != GEMMAR_SCALE_MX32)
+    if (!known_scale_kind(scale_kind))
         return GEMMAR_ERR_ARG;
     return shape_rules(P, M, N, K, bands, scale_kind);
 }
@@ -302,6 +331,12 @@ GEMMAR_API int gemm_blockscale_fp8(gemmar_ctx *ctx, const uint8_t *A, const floa
                                    void *stream)
 {
     return gemm_single(ctx, A, sa, B, sb, C, c_dtype, M, N, K, GEMMAR_SCALE_BLOCK128, stream);
+}
+
+GEMMAR_API int gemm_ptpc_fp8(gemmar_ctx *ctx, const uint8_t *A, const float *sa, const uint8_t *B, const float *sb,
+                             void *C, int c_dtype, int64_t M, int64_t N, int64_t K, void *stream)
+{
+    return gemm_single(ctx, A, sa, B, sb, C, c_dtype, M, N, K, GEMMAR_SCALE_PTPC, stream);
 }
 
 GEMMAR_API int gemm_mxfp8(gemmar_ctx *ctx, const uint8_t *A, const uint8_t *ea, const uint8_t *B, const uint8_t *eb,
@@ -400,7 +435,7 @@ GEMMAR_API int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A
     int rc = check_ctx(ctx);
     if (rc)
         return rc;
-    if (!A || !sa || !B || !sb || !out || (scale_kind != GEMMAR_SCALE_BLOCK128 && scale_kind != GEMMAR_SCALE_MX32))
+    if (!A || !sa || !B || !sb || !out || !known_scale_kind(scale_kind))
         return GEMMAR_ERR_ARG;
     if (bands == 0)
         bands = P;
@@ -416,8 +451,11 @@ GEMMAR_API int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A
         return GEMMAR_ERR_ALIGN;
     // on-chip partial sums: mx on the mx kernel, blockscale on the CTA-pair kernel
     // (N % 256 == 0); other blockscale shapes take the band path, whose bits they reproduce
-    const bool onchip = (flags & GEMMAR_FUSE_ONCHIP) &&
-                        (scale_kind == GEMMAR_SCALE_MX32 || plan_blockscale(P, M, N, K, bands, 2, ctx->num_sms, 1).pair);
+    // ptpc applies its scales after the whole K of a slice, so its only in-tile
+    // reduction is the on-chip one (GEMMAR_FUSE_SLICES takes it too)
+    const bool onchip = ((flags & GEMMAR_FUSE_ONCHIP) ||
+                         (scale_kind == GEMMAR_SCALE_PTPC && (flags & GEMMAR_FUSE_SLICES))) &&
+                        (scale_kind != GEMMAR_SCALE_BLOCK128 || plan_blockscale(P, M, N, K, bands, 2, ctx->num_sms, 1).pair);
     const bool slices = onchip || ((flags & GEMMAR_FUSE_SLICES) != 0 && !(flags & GEMMAR_FUSE_ONCHIP));
     if (!slices && blocked_partial_floats(P, M, bands, N) > ctx->W_floats)
         return GEMMAR_ERR_WORKSPACE;
@@ -452,7 +490,7 @@ GEMMAR_API int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A
             bn = pl.bn;
             expected = pl.band_signals;
         } else {
-            bn = mx_tile_n(N);
+            bn = scale_kind == GEMMAR_SCALE_PTPC ? ptpc_tile_n(N) : mx_tile_n(N);
             const TileGrid g = make_grid(P, M, N, K, bands, bn);
             expected = (uint32_t)(g.mt_per_band * g.ntiles_n * P * 8);
         }

@@ -51,11 +51,16 @@ struct BsParams {
     uint64_t timeout_ns;
 };
 
+// Parameters of the whole-K kernel family (gemm_mx.cu): mxfp8 (native
+// block-scaled MMA, the scale images below) and ptpc (plain e4m3 MMA, one fp32
+// scale per row of A and per row of B applied to the tile in the epilogue).
 struct MxParams {
     CUtensorMap tmA[kMaxP];
     CUtensorMap tmB[kMaxP];
-    const uint8_t *sfa;      // repacked A scale words: [P][bands][mt_per_band][K/128][512 B]
-    const uint8_t *sfb;      // repacked B scale words: [P][N/BN][K/128][1024 B]
+    const uint8_t *sfa;      // mx: repacked A scale words: [P][bands][mt_per_band][K/128][512 B]
+    const uint8_t *sfb;      // mx: repacked B scale words: [P][N/BN][K/128][1024 B]
+    const float *pa[kMaxP];  // ptpc: per-token scales of A_p, [M]
+    const float *pb[kMaxP];  // ptpc: per-channel scales of B_p, [N]
     TileGrid g;
     GemmOut o;
     ptx::DevStatus *status;
@@ -65,9 +70,11 @@ struct MxParams {
 // GEMM launchers (bn: 256 or 128 for blockscale; 224 or 128 for mx).
 cudaError_t launch_gemm_blockscale(const BsParams &p, int bn, int grid, cudaStream_t s);
 cudaError_t launch_gemm_mx(const MxParams &p, int bn, int grid, cudaStream_t s);
+cudaError_t launch_gemm_ptpc(const MxParams &p, int bn, int grid, cudaStream_t s);
 // Register count each GEMM kernel was built with (the warp-role register split needs it).
 int gemm_blockscale_num_regs(int bn);
 int gemm_mx_num_regs(int bn);
+int gemm_ptpc_num_regs(int bn);
 int gemm_threads();
 
 // Blockscale launch plan: CTA pairs (gemm_blockscale_2sm.cu, 256 x 128 pair

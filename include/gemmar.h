@@ -71,8 +71,10 @@ enum {
 enum { GEMMAR_DTYPE_F32 = 0, GEMMAR_DTYPE_BF16 = 1 };
 
 /* Scale kinds. BLOCK128: fp32 A scales [M, K/128], fp32 B scales [N/128, K/128].
- * MX32: ue8m0 bytes (value 2^(byte-127)), A [M, K/32], B [N, K/32]. */
-enum { GEMMAR_SCALE_BLOCK128 = 0, GEMMAR_SCALE_MX32 = 1 };
+ * MX32: ue8m0 bytes (value 2^(byte-127)), A [M, K/32], B [N, K/32].
+ * PTPC: fp32 per-token A scales [M] and per-channel B scales [N] (one scale
+ * per row of A and of B over the whole K). */
+enum { GEMMAR_SCALE_BLOCK128 = 0, GEMMAR_SCALE_MX32 = 1, GEMMAR_SCALE_PTPC = 2 };
 
 /* Flags of gemmar_create and fused_gemm_reduce. */
 #define GEMMAR_FP8_WIRE        (1u << 0)  /* fused: per-row e4m3 quantise + dequantise of the output */
@@ -172,6 +174,19 @@ int gemm_blockscale_fp8(gemmar_ctx *ctx, const uint8_t *A, const float *sa, cons
                         void *stream);
 
 /*
+ * gemm_ptpc_fp8 -- C[M,N] = (sa[m]*sb[n]) * sum_k a[m,k]*b[n,k] for one K-slice:
+ * the "ptpc" quantisation the MORI benchmark runs by default ("Negative
+ * results", the paragraph on pinning `--quant`), read as per-token A scales and
+ * per-output-channel B scales.  The MMA accumulates the whole K in TMEM (no
+ * promotion); the epilogue multiplies by the fp32 product sa[m]*sb[n].
+ *   A: e4m3 [M,K]; sa: fp32 [M]; B: e4m3 [N,K]; sb: fp32 [N];
+ *   C: [M,N] of c_dtype.  Shape rules as gemmar_supports with P = bands = 1.
+ */
+int gemm_ptpc_fp8(gemmar_ctx *ctx, const uint8_t *A, const float *sa, const uint8_t *B,
+                  const float *sb, void *C, int c_dtype, int64_t M, int64_t N, int64_t K,
+                  void *stream);
+
+/*
  * gemm_mxfp8 -- C[M,N] = sum_g 2^(ea[m,g]+eb[n,g]-254) * sum_{k in g} a[m,k]*b[n,k]
  * for one K-slice, on the native block-scaled MMA (tcgen05 kind::mxf8f6f4,
  * one ue8m0 scale per 32 of K); the mxfp8 wo_b of sglang pull request #43480.
@@ -269,10 +284,13 @@ int quant_mx_e4m3(gemmar_ctx *ctx, const float *x, int64_t R, int64_t C, uint8_t
  * W_1) + W_2) + ..., in fp32 before the single bf16 rounding, without the
  * 2 x P*M*N*4 bytes of partial traffic.  Blockscale (N % 256 == 0, a GPU that
  * runs CTA pairs) runs on the CTA-pair kernel, the running sum in shared
- * memory: bit-equal to the band path of a GEMMAR_CTA_PAIR context.  mx runs on
- * the mx kernel, each slice accumulating in a TMEM buffer of its own and the
- * running sum in registers: bit-equal to the mx band path.  Other blockscale
- * shapes take the band path.  Takes precedence over GEMMAR_FUSE_SLICES.
+ * memory: bit-equal to the band path of a GEMMAR_CTA_PAIR context.  mx and
+ * ptpc run on the whole-K kernel, each slice accumulating in a TMEM buffer of
+ * its own (ptpc: then scaled) and the running sum in registers: bit-equal to
+ * their band path.  Other blockscale shapes take the band path.  Takes
+ * precedence over GEMMAR_FUSE_SLICES, which for ptpc means the same as
+ * GEMMAR_FUSE_ONCHIP (its scales apply after a slice's whole K, so no single
+ * chain over the slices exists).
  */
 int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A, const void *const *sa,
                       const uint8_t *const *B, const void *const *sb, int scale_kind,

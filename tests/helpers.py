@@ -32,6 +32,16 @@ def mx_operands(P, M, N, K, seed=0):
     return A, sa, B, sb
 
 
+def ptpc_operands(P, M, N, K, seed=0):
+    """Per-token A and per-channel B scales (one fp32 scale per row of each)."""
+    A, sa, B, sb = [], [], [], []
+    for p in range(P):
+        a, s = oracle.quant_ptpc(synthetic.normal(seed, synthetic.TID_A, p, (M, K)))
+        b, t = oracle.quant_ptpc(synthetic.normal(seed, synthetic.TID_B, p, (N, K), sigma=0.02))
+        A.append(a); sa.append(s); B.append(b); sb.append(t)
+    return A, sa, B, sb
+
+
 def rel_l2(x, ref):
     x = np.asarray(x, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)

@@ -158,3 +158,29 @@ def test_onchip_full_size_bit_equal_to_pair_band_path(g, headline):
         check_bf16_output(got, ref, f"on-chip P=8 M={M}")
     finally:
         ctx2.close()
+
+
+def test_fused_ptpc_full_size(g):
+    """ptpc at the headline shape: sampled rows against the oracle, the on-chip
+    sums bit-equal to the band path."""
+    from helpers import ptpc_operands
+    A, sa, B, sb = ptpc_operands(P, MMAX, N, K, seed=12)
+    torch.cuda.set_device(0)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    ctx = g.gemmar_create(0, MMAX, N, K, P)
+    try:
+        outs = []
+        for flags in (0, g.GEMMAR_FUSE_ONCHIP):
+            out = torch.empty((MMAX, N), dtype=torch.bfloat16, device="cuda")
+            g.fused_gemm_reduce(ctx, [dev(a) for a in A], [dev(s) for s in sa], [dev(b) for b in B],
+                                [dev(s) for s in sb], out, scale_kind=g.GEMMAR_SCALE_PTPC, bands=P, flags=flags)
+            torch.cuda.synchronize()
+            assert g.gemmar_status(ctx)[0] == 0
+            outs.append(out)
+        assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+        rows = sample_rows(MMAX, P, seed=13)
+        got = outs[0][torch.from_numpy(rows).cuda()].float().cpu().numpy()
+        ref, _ = oracle.gemm_reduce(A, sa, B, sb, 2, rows=rows)
+        check_bf16_output(got, ref, f"ptpc P=8 M={MMAX}")
+    finally:
+        ctx.close()

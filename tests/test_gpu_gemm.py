@@ -272,3 +272,37 @@ def test_onchip_on_default_context_matches_one_cta_band_path(g, ctx):
     check_bf16_output(onchip.float().cpu().numpy(), ref, "on-chip, default context")
     d = (onchip.view(torch.int16).int() - band.view(torch.int16).int()).abs()
     assert int(d.max()) <= 1
+
+
+# ------------------------------------------------------------ ptpc (per-token / per-channel scales)
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (200, 384, 512), (384, 768, 384), (1, 128, 256),
+                                   (256, 512, 1024)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_gemm_ptpc(g, ctx, M, N, K, out_dtype):
+    from helpers import ptpc_operands
+    A, sa, B, sb = ptpc_operands(1, M, N, K, seed=M + 3 * N + K)
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, 2)
+    C = torch.full((M, N), float("nan"), dtype=out_dtype, device="cuda")
+    g.gemm_ptpc_fp8(ctx, dev(A[0]), dev(sa[0]), dev(B[0]), dev(sb[0]), C)
+    status_ok(g, ctx)
+    if out_dtype == torch.float32:
+        check_f32_output(C.cpu().numpy(), ref, f"ptpc f32 {M}x{N}x{K}")
+    else:
+        check_bf16_output(C.float().cpu().numpy(), ref, f"ptpc bf16 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("P,M,N,K,bands", [(2, 256, 512, 256, 2), (3, 600, 384, 384, 3), (8, 1024, 256, 128, 8),
+                                           (4, 520, 1024, 256, 4), (1, 256, 256, 256, 1)])
+def test_fused_ptpc_band_onchip_bitwise(g, ctx, P, M, N, K, bands):
+    from helpers import ptpc_operands
+    A, sa, B, sb = ptpc_operands(P, M, N, K, seed=51 + P * M)
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, 2)
+    band = run_fused(g, ctx, A, sa, B, sb, g.GEMMAR_SCALE_PTPC, bands, flags=g.GEMMAR_DEBUG_CANARY)
+    rl = check_bf16_output(band.float().cpu().numpy(), ref, f"ptpc band P={P} M={M} N={N} K={K}")
+    assert rl < 2.35e-3
+    onchip = run_fused(g, ctx, A, sa, B, sb, g.GEMMAR_SCALE_PTPC, bands,
+                       flags=g.GEMMAR_FUSE_ONCHIP | g.GEMMAR_DEBUG_CANARY)
+    assert torch.equal(onchip.view(torch.int16), band.view(torch.int16))
+    slices = run_fused(g, ctx, A, sa, B, sb, g.GEMMAR_SCALE_PTPC, bands, flags=g.GEMMAR_FUSE_SLICES)
+    assert torch.equal(slices.view(torch.int16), band.view(torch.int16))
