@@ -259,11 +259,17 @@ def make_inputs(g, ctx, P, M, N, K, dev, seed, kind):
             t = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
             g.quant_blockscale_e4m3(ctx, x, 1, a, s)
             g.quant_blockscale_e4m3(ctx, w, 128, b, t)
-        else:
+        elif kind == 1:
             s = torch.empty((M, K // 32), dtype=torch.uint8, device=dev)
             t = torch.empty((N, K // 32), dtype=torch.uint8, device=dev)
             g.quant_mx_e4m3(ctx, x, a, s)
             g.quant_mx_e4m3(ctx, w, b, t)
+        else:
+            # ptpc: one scale per row of A (token) and of B (channel) -- the row codec
+            s = torch.empty((M,), dtype=torch.float32, device=dev)
+            t = torch.empty((N,), dtype=torch.float32, device=dev)
+            g.rowquant_e4m3(ctx, x, a, s)
+            g.rowquant_e4m3(ctx, w, b, t)
         del x, w
         A.append(a); sa.append(s); B.append(b); sb.append(t)
     torch.cuda.synchronize(dev)
@@ -418,6 +424,33 @@ def run_ours(args, rank, world, local_rank):
                       "onchip_note": "GEMMAR_FUSE_ONCHIP: a TMEM buffer per slice, running sum in registers; "
                                      "bit-equal to the mx band path (tests)"}
     del Amx, eam, Bmx, ebm
+    torch.cuda.empty_cache()
+
+    # ---- the ptpc quantisation (per-token A, per-channel B fp32 scales), P = 8
+    Apt, spa, Bpt, spb = make_inputs(g, ctx, P, M, N, K, dev, seed=11 + rank, kind=2)
+    step_pt = lambda: g.fused_gemm_reduce(ctx, Apt, spa, Bpt, spb, out, scale_kind=g.GEMMAR_SCALE_PTPC, bands=P)
+    for _ in range(3):
+        step_pt()
+    g.gemmar_set_phase_timing(ctx, True)
+    ms_pt = time_steps(step_pt, max(5, args.steps // 2), stream)
+    g.gemmar_set_phase_timing(ctx, False)
+    pph, pcalls = g.gemmar_phase_times(ctx)
+    pt_gemm_ms = pph["gemm"] / max(pcalls, 1)
+    step_pt_oc = lambda: g.fused_gemm_reduce(ctx, Apt, spa, Bpt, spb, out, scale_kind=g.GEMMAR_SCALE_PTPC,
+                                             bands=P, flags=g.GEMMAR_FUSE_ONCHIP)
+    for _ in range(2):
+        step_pt_oc()
+    ms_pt_oc = time_steps(step_pt_oc, max(5, args.steps // 2), stream)
+    extra["ptpc"] = {"workload": "P=8 slices of M=16384 N=7168 K=2048, fp32 per-token A and per-channel B scales",
+                     "us_per_layer": ms_pt * 1e3,
+                     "gemm_us": pt_gemm_ms * 1e3,
+                     "gemm_tflops": fl / (pt_gemm_ms * 1e-3) / 1e12,
+                     "gemm_frac_of_fp8_peak": fl / (pt_gemm_ms * 1e-3) / 1e12 / fp8_peak,
+                     "onchip_us_per_layer": ms_pt_oc * 1e3,
+                     "onchip_tflops": fl / (ms_pt_oc * 1e-3) / 1e12,
+                     "note": "no per-K-block promotion: the whole K accumulates in TMEM, scaled once per "
+                             "tile; on-chip bit-equal to the ptpc band path (tests)"}
+    del Apt, spa, Bpt, spb
     torch.cuda.empty_cache()
 
     # ---- end to end through the public API: every step copies its activations
