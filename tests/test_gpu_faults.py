@@ -55,23 +55,28 @@ def test_host_side_errors_launch_nothing(g):
     ctx.close()
 
 
-def test_unsignalled_band_times_out_cleanly(g):
+@pytest.mark.parametrize("kind,create_flags", [(0, 0), (0, "pair"), (1, 0), (2, 0)],
+                         ids=["blockscale", "blockscale-cta-pair", "mx", "ptpc"])
+def test_unsignalled_band_times_out_cleanly(g, kind, create_flags):
+    from helpers import mx_operands, ptpc_operands
     torch.cuda.set_device(0)
-    ctx = g.gemmar_create(0, 256, 512, 256, 2, flags=g.GEMMAR_NO_SELF_TEST, wait_timeout_ns=50_000_000)
-    A, sa, B, sb = blockscale_operands(2, 256, 512, 256, seed=2)
+    cflags = g.GEMMAR_NO_SELF_TEST | (g.GEMMAR_CTA_PAIR if create_flags == "pair" else 0)
+    ctx = g.gemmar_create(0, 256, 512, 256, 2, flags=cflags, wait_timeout_ns=50_000_000)
+    make = {0: blockscale_operands, 1: mx_operands, 2: ptpc_operands}[kind]
+    A, sa, B, sb = make(2, 256, 512, 256, seed=2)
     dA, dsa, dB, dsb = [dev(a) for a in A], [dev(s) for s in sa], [dev(b) for b in B], [dev(s) for s in sb]
     out = torch.empty((256, 512), dtype=torch.bfloat16, device="cuda")
-    g.fused_gemm_reduce(ctx, dA, dsa, dB, dsb, out, flags=g.GEMMAR_FAULT_SKIP_BAND)
+    g.fused_gemm_reduce(ctx, dA, dsa, dB, dsb, out, scale_kind=kind, flags=g.GEMMAR_FAULT_SKIP_BAND)
     torch.cuda.synchronize()                    # the wait gave up: no hang, context still usable
     code, detail = g.gemmar_status(ctx)
     assert code == g.GEMMAR_ERR_TIMEOUT and detail == 7      # the reducer's band wait
     with pytest.raises(g.GemmarError) as e:     # sticky-disabled afterwards
-        g.fused_gemm_reduce(ctx, dA, dsa, dB, dsb, out)
+        g.fused_gemm_reduce(ctx, dA, dsa, dB, dsb, out, scale_kind=kind)
     assert e.value.code == g.GEMMAR_ERR_DISABLED
     ctx.close()
     # a fresh context on the same device works
-    ctx2 = g.gemmar_create(0, 256, 512, 256, 2, flags=g.GEMMAR_NO_SELF_TEST)
-    g.fused_gemm_reduce(ctx2, dA, dsa, dB, dsb, out)
+    ctx2 = g.gemmar_create(0, 256, 512, 256, 2, flags=cflags)
+    g.fused_gemm_reduce(ctx2, dA, dsa, dB, dsb, out, scale_kind=kind)
     torch.cuda.synchronize()
     assert g.gemmar_status(ctx2)[0] == 0
     ctx2.close()

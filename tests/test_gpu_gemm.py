@@ -306,3 +306,18 @@ def test_fused_ptpc_band_onchip_bitwise(g, ctx, P, M, N, K, bands):
     assert torch.equal(onchip.view(torch.int16), band.view(torch.int16))
     slices = run_fused(g, ctx, A, sa, B, sb, g.GEMMAR_SCALE_PTPC, bands, flags=g.GEMMAR_FUSE_SLICES)
     assert torch.equal(slices.view(torch.int16), band.view(torch.int16))
+
+
+def test_ptpc_zero_scales_give_exact_zeros(g, ctx):
+    from helpers import ptpc_operands
+    P, M, N, K = 3, 384, 512, 256
+    A, sa, B, sb = ptpc_operands(P, M, N, K, seed=61)
+    for p in range(P):
+        sa[p][17] = 0.0           # token 17 scaled to zero in every slice
+        sb[p][300] = 0.0          # channel 300 scaled to zero in every slice
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, 2)
+    for flags in (0, g.GEMMAR_FUSE_ONCHIP):
+        out = run_fused(g, ctx, A, sa, B, sb, g.GEMMAR_SCALE_PTPC, P, flags=flags | g.GEMMAR_DEBUG_CANARY)
+        o = out.float().cpu().numpy()
+        assert np.all(o[17] == 0) and np.all(o[:, 300] == 0)
+        check_bf16_output(o, ref, f"ptpc zero scales flags={flags}")
