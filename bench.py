@@ -559,16 +559,16 @@ def run_ours(args, rank, world, local_rank):
 
 def run_profile_case(args):
     """One warm-up and one measured call of a single configuration, for
-    profilers (ncu -k ... -s 1 -c 1): the fused layer (blockscale P=8 or mx
-    P=4 at M rows, with --flags), or the row codec alone on a [M, 7168] bf16
-    matrix (--codec).  No timing is printed; the exit status is the device
+    profilers (ncu -k ... -s 1 -c 1): the fused layer (blockscale or ptpc P=8,
+    mx P=4, at M rows, with --flags), or the row codec alone on a [M, 7168]
+    bf16 matrix (--codec).  No timing is printed; the exit status is the device
     status."""
     import torch
     import block_scaled_fp8_gemm_gb300 as g
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     M, N, K = args.m, N_HEAD, K_HEAD
-    kind = 1 if args.kind == "mx" else 0
+    kind = {"blockscale": 0, "mx": 1, "ptpc": 2}[args.kind]
     P = 4 if kind == 1 else P_HEAD
     ctx = g.gemmar_create(0, M, N, K, P, flags=g.GEMMAR_NO_SELF_TEST)
     if args.codec:
@@ -601,7 +601,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle leg")
     ap.add_argument("--profile-case", action="store_true",
                     help="single-shot case for profilers (see --kind, --m, --flags, --codec); prints nothing")
-    ap.add_argument("--kind", choices=("blockscale", "mx"), default="blockscale")
+    ap.add_argument("--kind", choices=("blockscale", "mx", "ptpc"), default="blockscale")
     ap.add_argument("--m", type=int, default=2048)
     ap.add_argument("--flags", type=int, default=0, help="fused_gemm_reduce flags (1 fp8 wire, 16 slice loop)")
     ap.add_argument("--codec", action="store_true", help="profile case: the row codec alone on [M, 7168] bf16")
