@@ -571,16 +571,22 @@ int self_test(gemmar_ctx *ctx)
     }
     std::vector<float> ones(std::max(sa_bytes, sb_bytes) / 4, 1.0f);
     std::vector<uint16_t> host(M * N);
-    for (int kind = 0; kind < 2 && rc == GEMMAR_OK; ++kind) {
+    // every scale kind, on the band path and with the partials summed on chip
+    for (int run = 0; run < 6 && rc == GEMMAR_OK; ++run) {
+        const int kind = run % 3;
+        const uint32_t flags = run < 3 ? 0u : GEMMAR_FUSE_ONCHIP;
         const uint16_t expect = (P * K == 256) ? 0x4380 : 0x4300;   // bf16 of 256 (P=2) or 128 (P=1)
         bool ok = cudaMemsetAsync(dA, 0x38, a_bytes, st) == cudaSuccess &&
                   cudaMemsetAsync(dB, 0x38, b_bytes, st) == cudaSuccess;
         if (kind == GEMMAR_SCALE_BLOCK128)
             ok = ok && cudaMemcpyAsync(dsa, ones.data(), M * (K / 128) * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
                  cudaMemcpyAsync(dsb, ones.data(), (N / 128) * (K / 128) * 4, cudaMemcpyHostToDevice, st) == cudaSuccess;
-        else
+        else if (kind == GEMMAR_SCALE_MX32)
             ok = ok && cudaMemsetAsync(dsa, 127, M * (K / 32), st) == cudaSuccess &&
                  cudaMemsetAsync(dsb, 127, N * (K / 32), st) == cudaSuccess;
+        else
+            ok = ok && cudaMemcpyAsync(dsa, ones.data(), M * 4, cudaMemcpyHostToDevice, st) == cudaSuccess &&
+                 cudaMemcpyAsync(dsb, ones.data(), N * 4, cudaMemcpyHostToDevice, st) == cudaSuccess;
         ok = ok && cudaMemsetAsync(dout, 0, out_bytes, st) == cudaSuccess;
         if (!ok) {
             rc = GEMMAR_ERR_CUDA;
@@ -588,7 +594,7 @@ int self_test(gemmar_ctx *ctx)
         }
         const uint8_t *As[2] = {dA, dA}, *Bs[2] = {dB, dB};
         const void *SA[2] = {dsa, dsa}, *SB[2] = {dsb, dsb};
-        rc = fused_gemm_reduce(ctx, P, As, SA, Bs, SB, kind, M, N, K, P, 0u, dout, st);
+        rc = fused_gemm_reduce(ctx, P, As, SA, Bs, SB, kind, M, N, K, P, flags, dout, st);
         if (rc == GEMMAR_OK && cudaStreamSynchronize(st) != cudaSuccess)
             rc = GEMMAR_ERR_CUDA;
         if (rc == GEMMAR_OK)

@@ -103,7 +103,8 @@ enum { GEMMAR_SCALE_BLOCK128 = 0, GEMMAR_SCALE_MX32 = 1, GEMMAR_SCALE_PTPC = 2 }
  * "Worth a reviewer's attention", last item.)  Rules:
  *   M >= 1; 1 <= P <= GEMMAR_MAX_P; 1 <= bands <= min(M, 1024) and M % bands == 0;
  *   BLOCK128: N % 128 == 0 (the B scale block); MX32: N % 128 == 0 or N % 224 == 0;
- *   K % 128 == 0 (both scale kinds: one MMA stage is 128 of K);
+ *   PTPC: N % 128 == 0;
+ *   K % 128 == 0 (every scale kind: one MMA stage is 128 of K);
  *   N <= 65536, K <= 65536, M <= 2^24.
  * Returns GEMMAR_OK or GEMMAR_ERR_SHAPE / GEMMAR_ERR_ARG.  Needs no GPU.
  */
@@ -120,8 +121,9 @@ int gemmar_supports(int P, int64_t M, int64_t N, int64_t K, int bands, int scale
  * reviewer's attention": the window is sized from the chunked-prefill
  * ceiling, not from the first request).  wait_timeout_ns bounds every
  * device-side wait (0 = 2 s).  Unless GEMMAR_NO_SELF_TEST is set, runs the
- * fused path once on a closed-form case (unit codes and scales: every output
- * equals P*K) under that deadline and fails with GEMMAR_ERR_DEVICE on a
+ * fused path on a closed-form case (unit codes and scales: every output
+ * equals P*K) for every scale kind, on the band path and with the partials
+ * summed on chip, under that deadline, and fails with GEMMAR_ERR_DEVICE on a
  * mismatch (the pages' self_test(), sglang pull request #40757).
  * On success *out owns device memory until gemmar_destroy.
  */
