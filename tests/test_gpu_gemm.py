@@ -321,3 +321,18 @@ def test_ptpc_zero_scales_give_exact_zeros(g, ctx):
         o = out.float().cpu().numpy()
         assert np.all(o[17] == 0) and np.all(o[:, 300] == 0)
         check_bf16_output(o, ref, f"ptpc zero scales flags={flags}")
+
+
+@pytest.mark.parametrize("kind", [0, 1, 2])
+def test_fp8_wire_after_onchip_equals_wire_after_band_path(g, ctx, ctx_pair, kind):
+    # the wire codec runs on the reduced rows, which the on-chip sums reproduce bit for bit
+    from helpers import ptpc_operands
+    P, M, N, K = 4, 512, 512, 256
+    make = {0: blockscale_operands, 1: mx_operands, 2: ptpc_operands}[kind]
+    A, sa, B, sb = make(P, M, N, K, seed=71 + kind)
+    c = ctx_pair if kind == 0 else ctx
+    band = run_fused(g, c, A, sa, B, sb, kind, P, flags=g.GEMMAR_FP8_WIRE)
+    onchip = run_fused(g, c, A, sa, B, sb, kind, P, flags=g.GEMMAR_FP8_WIRE | g.GEMMAR_FUSE_ONCHIP)
+    assert torch.equal(onchip.view(torch.int16), band.view(torch.int16))
+    ref, ref16 = oracle.gemm_reduce(A, sa, B, sb, kind)
+    assert rel_l2(onchip.float().cpu().numpy(), ref) <= 3e-2
