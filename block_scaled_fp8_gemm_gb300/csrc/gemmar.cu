@@ -24,7 +24,7 @@ struct gemmar_ctx {
     int max_P = 0;
     uint32_t flags = 0;
     uint64_t timeout_ns = 0;
-    float *W = nullptr;               // fp32 partials, max_P * max_M * N
+    float *W = nullptr;               // fp32 partials, max_P * (max_M + 128 * max_P) * N (tile-blocked)
     int64_t W_floats = 0;
     uint32_t *band_done = nullptr;    // kMaxBands counters
     ptx::DevStatus *status = nullptr;
