@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
                     mbar_arrive_expect_tx(full + stage, C::kStageBytes);
                     tma_load_2d(smem + C::kOffA + stage * C::kABytes, &prm.tmA[p], full + stage, kb * 128, tc.m0);
                     tma_load_2d(smem + C::kOffB + stage * C::kBBytes, &prm.tmB[p], full + stage, kb * 128, tc.n0);
+                    ++issued;
                     if (++stage == C::kStages) {
                         stage = 0;
                         ph ^= 1;
