@@ -320,14 +320,32 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
     sampler.active = True
+    t_timed = time.perf_counter()
     ms = time_steps(step, args.steps, stream)
+    t_timed = time.perf_counter() - t_timed
+    g.gemmar_set_phase_timing(ctx, False)
+    phases, ncalls = g.gemmar_phase_times(ctx)
+    ov_blocks, all_blocks = g.gemmar_overlap_stats(ctx)   # of the last timed step
+    clock_note = None
+    if t_timed < 0.5:
+        # the timed steps ended within a few nvidia-smi periods: keep the same step
+        # running, untimed, so the clocks are read under this load
+        extra_steps = 0
+        t_end = time.perf_counter() + 0.5
+        while time.perf_counter() < t_end:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize()
+            extra_steps += 20
+        clock_note = (f"timed region {t_timed * 1e3:.0f} ms: clocks sampled over it and {extra_steps} "
+                      "further untimed steps of the same workload")
     sampler.active = False
     if world > 1:
         dist.barrier()
-    g.gemmar_set_phase_timing(ctx, False)
-    phases, ncalls = g.gemmar_phase_times(ctx)
     sampler.stop()
     clocks = sampler.summary()
+    if clock_note:
+        clocks["note"] = clock_note
     code, detail = g.gemmar_status(ctx)
     if code != 0:
         raise RuntimeError(f"device status {g.STATUS_NAMES.get(code)} at site {detail}")
@@ -339,8 +357,28 @@ def run_ours(args, rank, world, local_rank):
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]       # dense fp8 = 2 x bf16 (4.5 / 2.25 nominal)
     gemm_tflops = fl / (gemm_ms * 1e-3) / 1e12
     reduce_bytes = P * M * N * 4 + M * N * 2
-    reduce_gbs = reduce_bytes / (reduce_ms * 1e-3) / 1e9
+    # the reduce kernel after the GEMM sums the blocks the GEMM's reducer warps left
+    tail_share = 1.0 - ov_blocks / all_blocks if all_blocks else 1.0
+    tail_gbs = tail_share * reduce_bytes / (reduce_ms * 1e-3) / 1e9
     extra = {}
+
+    # ---- the same layer with the whole reduce after the GEMM (GEMMAR_SERIAL_REDUCE):
+    # band_reduce over every block, timed on its own
+    step_se = lambda: g.fused_gemm_reduce(ctx, A, sa, B, sb, out, bands=P, flags=g.GEMMAR_SERIAL_REDUCE)
+    for _ in range(2):
+        step_se()
+    g.gemmar_set_phase_timing(ctx, True)
+    ms_se = time_steps(step_se, max(5, args.steps // 2), stream)
+    g.gemmar_set_phase_timing(ctx, False)
+    sph, scalls = g.gemmar_phase_times(ctx)
+    se_gemm_ms = sph["gemm"] / max(scalls, 1)
+    se_reduce_ms = sph["reduce"] / max(scalls, 1)
+    reduce_gbs = reduce_bytes / (se_reduce_ms * 1e-3) / 1e9
+    extra["serial_reduce_layer"] = {
+        "us_per_layer": ms_se * 1e3, "gemm_us": se_gemm_ms * 1e3, "reduce_us": se_reduce_ms * 1e3,
+        "gemm_frac_of_fp8_peak": fl / (se_gemm_ms * 1e-3) / 1e12 / fp8_peak,
+        "note": "GEMMAR_SERIAL_REDUCE: the GEMM reduces nothing while it runs; band_reduce sums every "
+                "block after it (same output bits)"}
 
     # ---- the fp8 wire layer (config 3) and the row codec alone
     step_wire = lambda: g.fused_gemm_reduce(ctx, A, sa, B, sb, out, bands=P, flags=g.GEMMAR_FP8_WIRE)
@@ -535,12 +573,19 @@ def run_ours(args, rank, world, local_rank):
             "tflops_per_gpu": fl / (ms * 1e-3) / 1e12,
             "frac_of_fp8_peak": fl / (ms * 1e-3) / 1e12 / fp8_peak,
             "phases_us": {"gemm": gemm_ms * 1e3, "reduce": reduce_ms * 1e3},
+            "overlap": {"blocks_reduced_during_gemm": ov_blocks, "blocks": all_blocks,
+                        "share": ov_blocks / all_blocks if all_blocks else 0.0,
+                        "tail_reduce_us": reduce_ms * 1e3, "tail_reduce_GB/s": tail_gbs,
+                        "what": "spare warps of the GEMM kernel sum 32 x 32 output blocks of completed bands "
+                                "while it runs; band_reduce after it sums the rest"},
             "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
                          "frac": gemm_tflops / fp8_peak, "traffic": committed_traffic(),
-                         "kernel": "gemm_blockscale_kernel<256> (fused, band-ordered fp32 partials)",
+                         "kernel": "gemm_blockscale_kernel<256> (fused, band-ordered fp32 partials, "
+                                   "in-kernel reduce of completed bands)",
                          "peak_note": f"2 x bf16 sustained of {peaks['source']} peaks (fp8/bf16 nominal 4.5/2.25)"},
-            "band_reduce": {"us": reduce_ms * 1e3, "GB/s": reduce_gbs, "bytes": reduce_bytes,
-                            "frac_of_measured_hbm": reduce_gbs / peaks["hbm_gbs"]},
+            "band_reduce": {"us": se_reduce_ms * 1e3, "GB/s": reduce_gbs, "bytes": reduce_bytes,
+                            "frac_of_measured_hbm": reduce_gbs / peaks["hbm_gbs"],
+                            "what": "every block, after the GEMM (the GEMMAR_SERIAL_REDUCE leg)"},
             **extra,
             "e2e": {"value": replica_tflops(world, fl, e2e_ms), "unit": "TFLOP/s",
                     "us_per_layer": e2e_ms * 1e3, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -54,6 +54,7 @@ GEMMAR_NO_SELF_TEST = 1 << 3
 GEMMAR_FUSE_SLICES = 1 << 4
 GEMMAR_CTA_PAIR = 1 << 5
 GEMMAR_FUSE_ONCHIP = 1 << 6
+GEMMAR_SERIAL_REDUCE = 1 << 7
 GEMMAR_MAX_P = 8
 GEMMAR_NOALLOC_MAX_PARTIALS = 8 * 1024 * 1024
 
@@ -72,6 +73,7 @@ _SIGS = {
     "gemmar_workspace_bytes": (_I64, [_P]),
     "gemmar_set_phase_timing": (_I, [_P, _I]),
     "gemmar_phase_times": (_I, [_P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(_I)]),
+    "gemmar_overlap_stats": (_I, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "gemm_blockscale_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P]),
     "gemm_mxfp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P]),
     "gemm_ptpc_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P]),
@@ -212,6 +214,15 @@ def gemmar_phase_times(ctx: Context):
     calls = ctypes.c_int(0)
     _check(_lib.gemmar_phase_times(ctx.handle, ms, ctypes.byref(calls)), "gemmar_phase_times")
     return {PHASE_NAMES[i]: float(ms[i]) for i in range(GEMMAR_NUM_PHASES)}, int(calls.value)
+
+
+def gemmar_overlap_stats(ctx: Context):
+    """(blocks summed by the GEMM kernel while it ran, all 32 x 32 output blocks)
+    of the last fused band-path call; call after its work completed."""
+    ov = ctypes.c_int64(0)
+    tot = ctypes.c_int64(0)
+    _check(_lib.gemmar_overlap_stats(ctx.handle, ctypes.byref(ov), ctypes.byref(tot)), "gemmar_overlap_stats")
+    return int(ov.value), int(tot.value)
 
 
 def _cdtype(C: torch.Tensor) -> int:

@@ -156,6 +156,168 @@ struct BandSignals {
     }
 };
 
+// ---------------------------------------------------------------------------
+// In-kernel band reduce: one warp of a GEMM CTA sums retired bands while the
+// CTA's other warps keep computing tiles.  It works on 32-row x 32-column
+// blocks of the blocked partials (numbered within a band as in
+// band_reduce_blocked_kernel: column chunk fastest, then lane quarter, then
+// tile) and claims them with an atomic add on the band's own counter, and only
+// in bands whose retire count is complete, so it never waits on a block that
+// other CTAs have still to write: while the next band is incomplete it polls,
+// and it leaves as soon as its own CTA's epilogue warps are done (the band
+// reduce kernel launched after the GEMM takes, in every band, the blocks from
+// the final counter value on).  A block is read in four quarters (two 16-byte
+// column units of each lane's row, all P slices) through a four-stage cp.async
+// ring in shared memory; each lane loads and sums only its own row, so the ring
+// needs no warp barrier.  The arithmetic is that of the band reduce:
+// ((W_0 + W_1) + W_2) + ..., fp32, then bf16 RN.
+// ---------------------------------------------------------------------------
+constexpr int kReduceRingStages = 4;
+constexpr int kReduceRingBytes = kReduceRingStages * 8 * 1024;   // at two units per item, P <= 8
+
+struct BandClaim {
+    int band = 0;                // lowest band that may still have unclaimed blocks
+    int ready_upto = -1;         // bands <= ready_upto have been seen complete
+    uint32_t ahead = 0xFFFFFFFFu; // index taken in `band` by a claim issued one block early
+};
+
+// Lane 0 claims the next block of a complete band (band * bpb + index); -1
+// when this CTA's epilogue has finished, every band is claimed, or the poll ran
+// out of time.  After a successful claim the next one is issued at once (the
+// atomic's round trip then overlaps the block's copies); its index, if inside
+// the band, is a claimed block and is always returned by the next call.
+__device__ __forceinline__ int claim_retired_block(const GemmOut &o, const TileGrid &g, uint32_t bpb, BandClaim &cl,
+                                                   const volatile int *epi_done, int epi_warps, uint64_t timeout_ns)
+{
+    int blk = -1;
+    if ((threadIdx.x & 31) == 0) {
+        if (cl.ahead != 0xFFFFFFFFu) {
+            const uint32_t r = cl.ahead;
+            cl.ahead = 0xFFFFFFFFu;
+            if (r < bpb)
+                blk = (int)((uint32_t)cl.band * bpb + r);
+            else
+                ++cl.band;   // this band is all claimed
+        }
+        const uint64_t t0 = ptx::globaltimer();
+        while (blk < 0 && cl.band < g.bands) {
+            // once this CTA's tiles are all stored, the rest is the reduce kernel's: it
+            // starts when every CTA has left, and runs on all of each SM's warps
+            if (*epi_done >= epi_warps)
+                break;
+            if (cl.band > cl.ready_upto) {
+                if (ptx::ld_acquire(o.band_done + cl.band) < o.band_expected) {
+                    if (ptx::globaltimer() - t0 > timeout_ns)
+                        break;
+                    __nanosleep(1024);
+                    continue;
+                }
+                cl.ready_upto = cl.band;
+            }
+            const uint32_t r = atomicAdd(o.reduce_next + cl.band, 1u);
+            if (r < bpb)
+                blk = (int)((uint32_t)cl.band * bpb + r);
+            else
+                ++cl.band;
+        }
+        if (blk >= 0 && *epi_done < epi_warps)
+            cl.ahead = atomicAdd(o.reduce_next + cl.band, 1u);   // cl.band is complete
+    }
+    return __shfl_sync(0xffffffffu, blk, 0);
+}
+
+// UNITS: 16-byte column units of each lane's row per item (2: a block is four
+// items of P x 1 KB; 1: eight items of P x 512 B).  ring: shared address of
+// kReduceRingStages * UNITS * 4 KB (16-byte aligned) that nothing else uses while
+// the reducer runs.  Whole warp calls.
+template <int UNITS>
+__device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGrid &g, int bn, uint32_t ring,
+                                                  const volatile int *epi_done, int epi_warps, uint64_t timeout_ns)
+{
+    constexpr int IPB = 8 / UNITS;                      // items per block
+    constexpr int STAGE = kMaxP * UNITS * 512;          // bytes per ring stage
+    const int lane = threadIdx.x & 31;
+    const int P = g.P;
+    const int nchunk = bn / 32;
+    const int64_t tiles_per_band = (int64_t)g.mt_per_band * g.ntiles_n;
+    const uint32_t bpb = (uint32_t)(tiles_per_band * 4 * nchunk);
+    const int64_t tile_f4 = 128 * (int64_t)bn / 4;
+    const int64_t slice_f4 = tiles_per_band * tile_f4;
+    const float4 *W = reinterpret_cast<const float4 *>(o.out);
+    int blk_even = -1, blk_odd = -1;   // block of items IPB*j..IPB*j+IPB-1: blk_even for even j, blk_odd for odd
+    bool more = true;
+    int issued = 0;
+    BandClaim cl;
+    // item k = units (k % IPB) * UNITS .. +UNITS-1 of its block, in ring stage k % kReduceRingStages
+    auto issue = [&](int k) {
+        const int j = (k / IPB) & 1;
+        if (more && k % IPB == 0) {
+            const int claimed = claim_retired_block(o, g, bpb, cl, epi_done, epi_warps, timeout_ns);
+            if (j)
+                blk_odd = claimed;
+            else
+                blk_even = claimed;
+            more = claimed >= 0;
+        }
+        if (more) {
+            const uint32_t blk = (uint32_t)(j ? blk_odd : blk_even);
+            const uint32_t b = blk / bpb, r = blk % bpb;
+            const int c = (int)(r % nchunk), q = (int)((r / nchunk) & 3);
+            const int64_t i = r / (4 * nchunk);
+            const float4 *src = W + ((int64_t)b * P * tiles_per_band + i) * tile_f4 +
+                                ((q * nchunk + c) * 8 + UNITS * (k % IPB)) * 32 + lane;
+            const uint32_t dst = ring + (k % kReduceRingStages) * STAGE + lane * 16;
+            for (int p = 0; p < P; ++p)
+#pragma unroll
+                for (int u = 0; u < UNITS; ++u)
+                    ptx::cp_async_cg16(dst + (p * UNITS + u) * 512, src + p * slice_f4 + u * 32);
+            ++issued;
+        }
+        ptx::cp_async_commit();   // one group per item slot, empty past the last item
+    };
+#pragma unroll 1
+    for (int k = 0; k < kReduceRingStages; ++k)
+        issue(k);
+#pragma unroll 1
+    for (int k = 0; k < issued; ++k) {
+        ptx::cp_async_wait<kReduceRingStages - 1>();   // this lane's copies of item k have landed
+        const uint32_t st = ring + (k % kReduceRingStages) * STAGE + lane * 16;
+        float a[4 * UNITS];
+#pragma unroll
+        for (int u = 0; u < UNITS; ++u) {
+            const uint4 w = ptx::ld_shared_v4(st + u * 512);
+            a[4 * u + 0] = __uint_as_float(w.x); a[4 * u + 1] = __uint_as_float(w.y);
+            a[4 * u + 2] = __uint_as_float(w.z); a[4 * u + 3] = __uint_as_float(w.w);
+        }
+        for (int p = 1; p < P; ++p)
+#pragma unroll
+            for (int u = 0; u < UNITS; ++u) {
+                const uint4 v = ptx::ld_shared_v4(st + (p * UNITS + u) * 512);
+                a[4 * u + 0] = a[4 * u + 0] + __uint_as_float(v.x); a[4 * u + 1] = a[4 * u + 1] + __uint_as_float(v.y);
+                a[4 * u + 2] = a[4 * u + 2] + __uint_as_float(v.z); a[4 * u + 3] = a[4 * u + 3] + __uint_as_float(v.w);
+            }
+        const uint32_t blk = (uint32_t)(((k / IPB) & 1) ? blk_odd : blk_even);
+        const uint32_t b = blk / bpb, r = blk % bpb;
+        const int c = (int)(r % nchunk), q = (int)((r / nchunk) & 3);
+        const int64_t i = r / (4 * nchunk);
+        const int mt = (int)(i / g.ntiles_n), nt = (int)(i % g.ntiles_n);
+        const int row = mt * 128 + q * 32 + lane;   // row within the band
+        if (row < g.rows_per_band) {
+            const int64_t m = (int64_t)b * g.rows_per_band + row;
+            const int64_t col = (int64_t)nt * bn + c * 32 + (k % IPB) * UNITS * 4;
+            if constexpr (UNITS == 2)
+                *reinterpret_cast<uint4 *>(o.red_out + m * g.N + col) =
+                    make_uint4(ptx::bf16x2_from_f32(a[0], a[1]), ptx::bf16x2_from_f32(a[2], a[3]),
+                               ptx::bf16x2_from_f32(a[4], a[5]), ptx::bf16x2_from_f32(a[6], a[7]));
+            else
+                *reinterpret_cast<uint2 *>(o.red_out + m * g.N + col) =
+                    make_uint2(ptx::bf16x2_from_f32(a[0], a[1]), ptx::bf16x2_from_f32(a[2], a[3]));
+        }
+        issue(k + kReduceRingStages);   // reuses this item's stage: this lane has read it
+    }
+    ptx::cp_async_wait<0>();
+}
+
 template <int N>
 __device__ __forceinline__ void setmaxnreg_dec()
 {

@@ -42,6 +42,7 @@ struct BsCfg {
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kTmemCols <= 512, "TMEM budget");
+    static_assert(kStagingBytes >= kReduceRingBytes, "the band reducer's ring reuses the staging");
 };
 
 constexpr int kThreads = 384;
@@ -61,6 +62,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
     uint64_t *final_bar = tempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+    volatile int *epi_done = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 8);   // epilogue warps finished
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -79,6 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
         }
         mbar_init(final_bar, 1);
         *abort_flag = 0;
+        *epi_done = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -174,6 +177,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
                     break;
                 }
             }
+        } else if (warp >= 2 && prm.o.out_mode == OUT_PARTIAL_F32 && prm.o.reduce_next != nullptr) {
+            // ------------------------------------------------ band reducers (the staging is
+            // unused when the epilogue writes blocked partials): one half of it each
+            band_reducer_warp<1>(prm.o, g, BN, smem_u32(smem + C::kOffStaging) + (warp - 2) * (kReduceRingBytes / 2),
+                                 epi_done, C::kEpiWarps, prm.timeout_ns);
         }
     } else {
         setmaxnreg_inc<kRegsHigh>();
@@ -286,6 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
         }
         if (ok)
             signals.flush(prm.o);
+        __syncwarp();
+        if (lane == 0)
+            atomicAdd(const_cast<int *>(epi_done), 1);
     }
 
     __syncwarp();

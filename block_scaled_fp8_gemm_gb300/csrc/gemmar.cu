@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -26,7 +27,7 @@ struct gemmar_ctx {
     uint64_t timeout_ns = 0;
     float *W = nullptr;               // fp32 partials, max_P * (max_M + 128 * max_P) * N (tile-blocked)
     int64_t W_floats = 0;
-    uint32_t *band_done = nullptr;    // kMaxBands counters
+    uint32_t *band_done = nullptr;    // kMaxBands retire counters, then as many claim counters
     ptx::DevStatus *status = nullptr;
     uint8_t *sfa = nullptr;           // mx repack images of A scales
     int64_t sfa_bytes = 0;
@@ -36,6 +37,10 @@ struct gemmar_ctx {
     float *wire_s = nullptr;          // fp8-wire row scales, max_M
     int disabled = 0;
     int64_t total_bytes = 0;
+    // the last fused band-path call, for gemmar_overlap_stats
+    int ov_bands = 0;                 // bands whose claim counters it used (0: no in-kernel reduce)
+    int64_t ov_bpb = 0;               // 32 x 32 blocks per band
+    int64_t ov_total = 0;             // blocks of the call
     // phase timing: one set of GEMMAR_NUM_PHASES + 1 events per recorded call
     int timing = 0;
     std::vector<cudaEvent_t> events;
@@ -302,6 +307,23 @@ GEMMAR_API int gemmar_status(gemmar_ctx *ctx, int *detail)
     return st.code;
 }
 
+GEMMAR_API int gemmar_overlap_stats(gemmar_ctx *ctx, int64_t *overlapped, int64_t *total)
+{
+    if (ctx == nullptr || overlapped == nullptr || total == nullptr)
+        return GEMMAR_ERR_ARG;
+    *overlapped = 0;
+    *total = ctx->ov_total;
+    if (ctx->ov_bands == 0)
+        return GEMMAR_OK;
+    std::vector<uint32_t> claimed((size_t)ctx->ov_bands);
+    if (cudaMemcpy(claimed.data(), ctx->band_done + ctx->ov_bands, sizeof(uint32_t) * claimed.size(),
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMMAR_ERR_CUDA;
+    for (uint32_t c : claimed)   // a counter can pass the band's block count by the claims that found it empty
+        *overlapped += std::min<int64_t>(c, ctx->ov_bpb);
+    return GEMMAR_OK;
+}
+
 GEMMAR_API int gemmar_destroy(gemmar_ctx *ctx)
 {
     if (ctx == nullptr)
@@ -462,6 +484,8 @@ GEMMAR_API int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A
     if ((flags & GEMMAR_FP8_WIRE) && M * N > ctx->max_M * ctx->N)
         return GEMMAR_ERR_WORKSPACE;
     cudaStream_t st = as_stream(stream);
+    ctx->ov_bands = 0;
+    ctx->ov_total = 0;
     if (slices) {
         // every tile accumulates all P slices itself: no partials, no band reduce
         if (flags & GEMMAR_DEBUG_CANARY)
@@ -472,30 +496,42 @@ GEMMAR_API int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A
             return rc;
         mark(ctx, GEMMAR_PHASE_REDUCE, st);
     } else {
-        CUDA_OK(cudaMemsetAsync(ctx->band_done, 0, sizeof(uint32_t) * bands, st));
-        if (flags & GEMMAR_DEBUG_CANARY) {
-            CUDA_OK(cudaMemsetAsync(ctx->W, 0xFF, sizeof(float) * (size_t)blocked_partial_floats(P, M, bands, N), st));
-            CUDA_OK(cudaMemsetAsync(out, 0xFF, sizeof(uint16_t) * (size_t)(M * N), st));
-        }
-        GemmOut o{ctx->W, ctx->band_done, OUT_PARTIAL_F32, (flags & GEMMAR_FAULT_SKIP_BAND) ? 0 : -1};
-        mark(ctx, GEMMAR_PHASE_GEMM, st);
-        if ((rc = run_gemm(ctx, P, A, sa, B, sb, scale_kind, M, N, K, bands, o, st)))
-            return rc;
-        mark(ctx, GEMMAR_PHASE_REDUCE, st);
         int bn;
         uint32_t expected;   // every epilogue warp signals once per retired tile
+        bool inkernel = false;   // the GEMM's reducer warps take the bands that retire while it runs
         if (scale_kind == GEMMAR_SCALE_BLOCK128) {
             const BsPlan pl = plan_blockscale(P, M, N, K, bands, 0, ctx->num_sms,
                                               (ctx->flags & GEMMAR_CTA_PAIR) ? 1 : 0);
             bn = pl.bn;
             expected = pl.band_signals;
+            inkernel = !pl.pair && !(flags & GEMMAR_SERIAL_REDUCE);
         } else {
             bn = scale_kind == GEMMAR_SCALE_PTPC ? ptpc_tile_n(N) : mx_tile_n(N);
             const TileGrid g = make_grid(P, M, N, K, bands, bn);
             expected = (uint32_t)(g.mt_per_band * g.ntiles_n * P * 8);
         }
-        CUDA_OK(launch_band_reduce_blocked(ctx->W, out, P, M, N, bands, bn, ctx->band_done, expected, ctx->status,
-                                           ctx->timeout_ns, ctx->num_sms * 8, st));
+        // band retire counters, then the reducer warps' per-band claim counters
+        uint32_t *claim = ctx->band_done + bands;
+        CUDA_OK(cudaMemsetAsync(ctx->band_done, 0, sizeof(uint32_t) * 2 * bands, st));
+        if (flags & GEMMAR_DEBUG_CANARY) {
+            CUDA_OK(cudaMemsetAsync(ctx->W, 0xFF, sizeof(float) * (size_t)blocked_partial_floats(P, M, bands, N), st));
+            CUDA_OK(cudaMemsetAsync(out, 0xFF, sizeof(uint16_t) * (size_t)(M * N), st));
+        }
+        GemmOut o{ctx->W, ctx->band_done, OUT_PARTIAL_F32, (flags & GEMMAR_FAULT_SKIP_BAND) ? 0 : -1,
+                  inkernel ? claim : nullptr, out, expected};
+        {
+            const int64_t mtpb = (M / bands + 127) / 128;
+            ctx->ov_bpb = mtpb * (N / bn) * 4 * (bn / 32);
+            ctx->ov_bands = inkernel ? bands : 0;
+            ctx->ov_total = inkernel ? ctx->ov_bpb * bands : 0;
+        }
+        mark(ctx, GEMMAR_PHASE_GEMM, st);
+        if ((rc = run_gemm(ctx, P, A, sa, B, sb, scale_kind, M, N, K, bands, o, st)))
+            return rc;
+        mark(ctx, GEMMAR_PHASE_REDUCE, st);
+        CUDA_OK(launch_band_reduce_blocked(ctx->W, out, P, M, N, bands, bn, ctx->band_done, expected,
+                                           inkernel ? claim : nullptr, ctx->status, ctx->timeout_ns,
+                                           ctx->num_sms * 8, st));
     }
     mark(ctx, GEMMAR_PHASE_QUANTIZE, st);
     if (flags & GEMMAR_FP8_WIRE)
@@ -663,7 +699,7 @@ GEMMAR_API int gemmar_create(gemmar_ctx **out, int device, int64_t max_M, int64_
             ctx->total_bytes += (int64_t)bytes;
     };
     alloc(reinterpret_cast<void **>(&ctx->W), sizeof(float) * (size_t)ctx->W_floats);
-    alloc(reinterpret_cast<void **>(&ctx->band_done), sizeof(uint32_t) * kMaxBands);
+    alloc(reinterpret_cast<void **>(&ctx->band_done), sizeof(uint32_t) * 2 * kMaxBands);   // + claim counters
     alloc(reinterpret_cast<void **>(&ctx->status), sizeof(ptx::DevStatus));
     alloc(reinterpret_cast<void **>(&ctx->sfa), (size_t)ctx->sfa_bytes);
     alloc(reinterpret_cast<void **>(&ctx->sfb), (size_t)ctx->sfb_bytes);

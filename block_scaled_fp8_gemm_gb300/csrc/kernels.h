@@ -38,6 +38,13 @@ struct GemmOut {
     uint32_t *band_done;     // per-band tile-retire counters (OUT_PARTIAL_F32)
     int out_mode;
     int skip_band;           // fault injection: this band is never signalled (-1: none)
+    // In-kernel band reduce (OUT_PARTIAL_F32 only; reduce_next == nullptr: off).  A
+    // warp of each CTA claims 32 x 32 blocks of retired bands from reduce_next[band]
+    // and writes their bf16 sums to red_out [M, N]; the blocks it leaves are reduced
+    // by the band reduce kernel that follows, in each band from the final count on.
+    uint32_t *reduce_next;   // [bands] claim counters, zero before the launch
+    uint16_t *red_out;
+    uint32_t band_expected;  // release signals that complete a band
 };
 
 struct BsParams {
@@ -106,8 +113,11 @@ cudaError_t launch_band_reduce(const float *W, uint16_t *out, int P, int64_t M, 
                                const uint32_t *band_done, uint32_t expected, ptx::DevStatus *status,
                                uint64_t timeout_ns, int grid_blocks, cudaStream_t s);
 // The same reduce over the fused path's tile-blocked partials (layout: epilogue.cuh).
+// claimed (device, [bands], may be nullptr): in band b the blocks below claimed[b]
+// were already reduced by the GEMM kernel's reducer warps (GemmOut::reduce_next).
 cudaError_t launch_band_reduce_blocked(const float *W, uint16_t *out, int P, int64_t M, int64_t N, int bands,
-                                       int bn, const uint32_t *band_done, uint32_t expected, ptx::DevStatus *status,
+                                       int bn, const uint32_t *band_done, uint32_t expected,
+                                       const uint32_t *claimed, ptx::DevStatus *status,
                                        uint64_t timeout_ns, int grid_blocks, cudaStream_t s);
 // Floats of blocked partials a fused call needs (ragged bands pad tiles to 128 rows).
 inline int64_t blocked_partial_floats(int P, int64_t M, int bands, int64_t N)

@@ -29,7 +29,7 @@ using namespace gemmar;
 // host code, only a stand-in for the symbol: the device address comes from
 // cudaGetSymbolAddress (see scratch_for_device).
 static __device__ __align__(256) float g_noalloc_partials[GEMMAR_NOALLOC_MAX_PARTIALS];
-static __device__ __align__(256) uint32_t g_noalloc_band_done[1024];
+static __device__ __align__(256) uint32_t g_noalloc_band_done[2 * 1024];   // retire, then claim counters
 static __device__ __align__(256) ptx::DevStatus g_noalloc_status;
 
 namespace {
@@ -145,19 +145,21 @@ extern "C" __attribute__((visibility("default"))) int fused_gemm_reduce_noalloc(
         prm.sb[p] = sb[p];
     }
     prm.g = pl.g;
-    prm.o = GemmOut{s->partials, s->band_done, OUT_PARTIAL_F32, -1};
+    // one-CTA plans run the GEMM kernel's reducer warps: claim counters after the retire counters
+    uint32_t *claim = pl.pair ? nullptr : s->band_done + bands;
+    prm.o = GemmOut{s->partials, s->band_done, OUT_PARTIAL_F32, -1, claim, out, pl.band_signals};
     prm.status = s->status;
     prm.timeout_ns = kTimeoutNs;
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // the counters and the status word keep the previous call's values: clear them
-    if (cudaMemsetAsync(s->band_done, 0, sizeof(uint32_t) * bands, st) != cudaSuccess ||
+    if (cudaMemsetAsync(s->band_done, 0, sizeof(uint32_t) * 2 * bands, st) != cudaSuccess ||
         cudaMemsetAsync(s->status, 0, sizeof(ptx::DevStatus), st) != cudaSuccess)
         return GEMMAR_ERR_CUDA;
     if (launch_blockscale(prm, pl, st) != cudaSuccess)
         return GEMMAR_ERR_CUDA;
     const uint32_t expected = pl.band_signals;
-    if (launch_band_reduce_blocked(s->partials, out, P, M, N, bands, bn, s->band_done, expected, s->status,
+    if (launch_band_reduce_blocked(s->partials, out, P, M, N, bands, bn, s->band_done, expected, claim, s->status,
                                    kTimeoutNs, s->num_sms * 8, st) != cudaSuccess)
         return GEMMAR_ERR_CUDA;
     return GEMMAR_OK;

@@ -481,6 +481,22 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
     return v;
 }
 
+// 16-byte global -> shared copy that bypasses L1 (cp.async, generic proxy):
+// the executing thread sees the data after a cp.async.wait_group that covers it.
+__device__ __forceinline__ void cp_async_cg16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// wait until at most N of this thread's committed cp.async groups are pending
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v)
 {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");

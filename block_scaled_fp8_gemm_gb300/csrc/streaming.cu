@@ -93,14 +93,17 @@ __global__ void __launch_bounds__(256) band_reduce_kernel(const float *__restric
 // the row's 64 bytes in registers; a warp-private shared transpose then
 // writes 8 rows x 64 bytes per store instruction.  Rows past the band end
 // (ragged bands) are not written.  Same arithmetic as band_reduce_kernel.
+// Blocks are numbered within a band (column chunk fastest, then lane quarter,
+// then tile); with `claimed` the kernel starts band b at block claimed[b], the
+// ones before it having been reduced by the GEMM kernel's reducer warps.
 // --------------------------------------------------------------------------
 template <int P>
 __global__ void __launch_bounds__(256) band_reduce_blocked_kernel(const float4 *__restrict__ W,
                                                                   uint16_t *__restrict__ out, int M, int N,
                                                                   int bands, int rows_per_band, int mt_per_band,
                                                                   int ntiles_n, int bn, const uint32_t *band_done,
-                                                                  uint32_t expected, DevStatus *status,
-                                                                  uint64_t timeout_ns)
+                                                                  uint32_t expected, const uint32_t *claimed,
+                                                                  DevStatus *status, uint64_t timeout_ns)
 {
     __shared__ int band_ok;
     __shared__ __align__(16) uint32_t stage[8][32 * 16];   // per warp: 32 rows x 64 bytes
@@ -133,7 +136,11 @@ __global__ void __launch_bounds__(256) band_reduce_blocked_kernel(const float4 *
             if (!band_ok)
                 return;
         }
-        for (int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp; blk < blocks_per_band; blk += warps_total) {
+        const int64_t blk0 = claimed != nullptr ? min64((int64_t)claimed[b], blocks_per_band) : 0;
+        if (blk0 >= blocks_per_band)
+            continue;
+        for (int64_t blk = blk0 + (int64_t)blockIdx.x * (blockDim.x >> 5) + warp; blk < blocks_per_band;
+             blk += warps_total) {
             const int c = (int)(blk % nchunk);
             const int q = (int)((blk / nchunk) % 4);
             const int64_t i = blk / (4 * nchunk);
@@ -559,8 +566,9 @@ cudaError_t launch_band_reduce(const float *W, uint16_t *out, int P, int64_t M, 
 }
 
 cudaError_t launch_band_reduce_blocked(const float *W, uint16_t *out, int P, int64_t M, int64_t N, int bands,
-                                       int bn, const uint32_t *band_done, uint32_t expected, DevStatus *status,
-                                       uint64_t timeout_ns, int grid_blocks, cudaStream_t s)
+                                       int bn, const uint32_t *band_done, uint32_t expected,
+                                       const uint32_t *claimed, DevStatus *status, uint64_t timeout_ns,
+                                       int grid_blocks, cudaStream_t s)
 {
     const int rpb = (int)(M / bands), mtpb = (rpb + 127) / 128, ntn = (int)(N / bn);
     const float4 *w4 = reinterpret_cast<const float4 *>(W);
@@ -568,7 +576,7 @@ cudaError_t launch_band_reduce_blocked(const float *W, uint16_t *out, int P, int
 #define GEMMAR_REDUCE_BLK_CASE(PP)                                                                                \
     case PP:                                                                                                      \
         band_reduce_blocked_kernel<PP><<<grid, block, 0, s>>>(w4, out, (int)M, (int)N, bands, rpb, mtpb, ntn, bn, \
-                                                              band_done, expected, status, timeout_ns);           \
+                                                              band_done, expected, claimed, status, timeout_ns);   \
         break;
     switch (P) {
         GEMMAR_REDUCE_BLK_CASE(1) GEMMAR_REDUCE_BLK_CASE(2) GEMMAR_REDUCE_BLK_CASE(3) GEMMAR_REDUCE_BLK_CASE(4)

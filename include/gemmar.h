@@ -93,6 +93,8 @@ enum { GEMMAR_SCALE_BLOCK128 = 0, GEMMAR_SCALE_MX32 = 1, GEMMAR_SCALE_PTPC = 2 }
                                              summed in the band reducer's order; bit-equal to the band
                                              path (blockscale: of a GEMMAR_CTA_PAIR context); see
                                              fused_gemm_reduce */
+#define GEMMAR_SERIAL_REDUCE   (1u << 7)  /* fused band path: the GEMM kernel reduces no band while it
+                                             runs; band_reduce sums every block after it (same bits) */
 
 /* Largest number of K-slices ("ranks") one call takes. */
 #define GEMMAR_MAX_P 8
@@ -160,6 +162,17 @@ enum { GEMMAR_PHASE_GEMM = 0, GEMMAR_PHASE_REDUCE = 1, GEMMAR_PHASE_QUANTIZE = 2
        GEMMAR_PHASE_DEQUANTIZE = 3, GEMMAR_NUM_PHASES = 4 };
 int gemmar_set_phase_timing(gemmar_ctx *ctx, int enable);
 int gemmar_phase_times(gemmar_ctx *ctx, float *ms, int *calls);
+
+/*
+ * gemmar_overlap_stats -- of the last fused_gemm_reduce band-path call on this
+ * context, *total = its 32-row x 32-column output blocks and *overlapped = how
+ * many of them the GEMM kernel's reducer warps summed while the GEMM was still
+ * running (the rest were summed by band_reduce after it).  Both 0 when the last
+ * fused call did not take the band path, or took it without the in-kernel
+ * reduce (GEMMAR_SERIAL_REDUCE, CTA-pair, mx and ptpc kernels).  Reads device
+ * memory with a synchronous copy: call after that call's work has completed.
+ */
+int gemmar_overlap_stats(gemmar_ctx *ctx, int64_t *overlapped, int64_t *total);
 
 /*
  * gemm_blockscale_fp8 -- C[M,N] = A[M,K] * B[N,K]^T for one K-slice, with
@@ -261,10 +274,14 @@ int quant_mx_e4m3(gemmar_ctx *ctx, const float *x, int64_t R, int64_t C, uint8_t
  * order whose epilogue stores each tile's fp32 partial into the context's
  * workspace W[band][p] and signals that band's counter as soon as the tile
  * retires (sglang pull request #40757, "What": the fused kernel hands each
- * row band over as soon as that band's tiles are done); then band_reduce
- * waits (bounded) for each band's counter and sums the P partials in fixed
- * order to bf16 out [M,N].  With GEMMAR_FP8_WIRE the reduced rows then go
- * through rowquant_e4m3 + rowdequant_e4m3 ("The fp8 wire").
+ * row band over as soon as that band's tiles are done).  On the one-CTA
+ * blockscale kernel two spare warps of every CTA take 32 x 32 output blocks
+ * of the bands already complete and sum them while the GEMM still runs (the
+ * hand-over overlapped with the compute, as the pages overlap their scatter
+ * with it); band_reduce then waits (bounded) for each band's counter and sums
+ * the P partials of the remaining blocks in the same fixed order to bf16 out
+ * [M,N].  With GEMMAR_FP8_WIRE the reduced rows then go through
+ * rowquant_e4m3 + rowdequant_e4m3 ("The fp8 wire").
  *   A[p], B[p], sa[p], sb[p]: HOST arrays of P device pointers; per slice as in
  *   gemm_blockscale_fp8 (scale_kind GEMMAR_SCALE_BLOCK128) or gemm_mxfp8
  *   (GEMMAR_SCALE_MX32).  bands: row bands (0 = P).  out: bf16 [M,N].

@@ -137,6 +137,19 @@ def test_fused_mx_full_size(g):
         ctx.close()
 
 
+@pytest.mark.parametrize("M", [4096, 16384])
+def test_band_path_overlap_full_size(g, headline, M):
+    """At the benchmark's shapes the GEMM kernel's reducer warps take a share of
+    the bands while the GEMM runs; the output is bit-equal to leaving every
+    block to band_reduce (GEMMAR_SERIAL_REDUCE)."""
+    over = run_fused(g, headline, M)
+    ov, tot = g.gemmar_overlap_stats(headline["ctx"])
+    assert tot == P * (M // P // 128) * (N // 256) * 4 * 8
+    assert 0 < ov < tot, (ov, tot)
+    serial = run_fused(g, headline, M, flags=g.GEMMAR_SERIAL_REDUCE)
+    assert torch.equal(over.view(torch.int16), serial.view(torch.int16))
+
+
 def test_onchip_full_size_bit_equal_to_pair_band_path(g, headline):
     """GEMMAR_FUSE_ONCHIP at the headline shape: sampled rows against the oracle,
     and the whole output bit-equal to the band path of the CTA-pair kernel."""
