@@ -50,6 +50,7 @@ struct MxCfg {
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kBBytes % 1024 == 0, "B tiles stay 1024-byte aligned");
+    static_assert(kStagingBytes >= kReduceRingBytes, "the band reducer's ring reuses the staging");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(PT ? 2 * BN <= 512 : 2 * BN <= (int)kSfaCol, "accumulators below the scale columns");
 };
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
     uint64_t *final_bar = tempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+    volatile int *epi_done = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 8);   // epilogue warps finished
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -117,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         }
         mbar_init(final_bar, 1);
         *abort_flag = 0;
+        *epi_done = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -245,6 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                 }
             }
         }
+      } else if (prm.o.out_mode == OUT_PARTIAL_F32 && prm.o.reduce_next != nullptr) {
+            // ------------------------------------------------ band reducers (warps 2-3; the
+            // staging is unused when the epilogue writes blocked partials): half of it each
+            band_reducer_warp<1>(prm.o, g, BN, smem_u32(smem + C::kOffStaging) + (warp - 2) * (kReduceRingBytes / 2),
+                                 epi_done, C::kEpiWarps, prm.timeout_ns);
       }
     } else {
         setmaxnreg_inc<kRegsHigh>();
@@ -363,6 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         }
         if (!exact)
             signals.flush(prm.o);
+        __syncwarp();
+        if (lane == 0)
+            atomicAdd(const_cast<int *>(epi_done), 1);
     }
 
     __syncwarp();

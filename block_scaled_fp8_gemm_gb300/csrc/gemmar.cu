@@ -509,6 +509,7 @@ GEMMAR_API int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A
             bn = scale_kind == GEMMAR_SCALE_PTPC ? ptpc_tile_n(N) : mx_tile_n(N);
             const TileGrid g = make_grid(P, M, N, K, bands, bn);
             expected = (uint32_t)(g.mt_per_band * g.ntiles_n * P * 8);
+            inkernel = !(flags & GEMMAR_SERIAL_REDUCE);
         }
         // band retire counters, then the reducer warps' per-band claim counters
         uint32_t *claim = ctx->band_done + bands;

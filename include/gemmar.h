@@ -169,7 +169,7 @@ int gemmar_phase_times(gemmar_ctx *ctx, float *ms, int *calls);
  * many of them the GEMM kernel's reducer warps summed while the GEMM was still
  * running (the rest were summed by band_reduce after it).  Both 0 when the last
  * fused call did not take the band path, or took it without the in-kernel
- * reduce (GEMMAR_SERIAL_REDUCE, CTA-pair, mx and ptpc kernels).  Reads device
+ * reduce (GEMMAR_SERIAL_REDUCE, or the CTA-pair kernel).  Reads device
  * memory with a synchronous copy: call after that call's work has completed.
  */
 int gemmar_overlap_stats(gemmar_ctx *ctx, int64_t *overlapped, int64_t *total);
@@ -274,13 +274,13 @@ int quant_mx_e4m3(gemmar_ctx *ctx, const float *x, int64_t R, int64_t C, uint8_t
  * order whose epilogue stores each tile's fp32 partial into the context's
  * workspace W[band][p] and signals that band's counter as soon as the tile
  * retires (sglang pull request #40757, "What": the fused kernel hands each
- * row band over as soon as that band's tiles are done).  On the one-CTA
- * blockscale kernel two spare warps of every CTA take 32 x 32 output blocks
- * of the bands already complete and sum them while the GEMM still runs (the
- * hand-over overlapped with the compute, as the pages overlap their scatter
- * with it); band_reduce then waits (bounded) for each band's counter and sums
- * the P partials of the remaining blocks in the same fixed order to bf16 out
- * [M,N].  With GEMMAR_FP8_WIRE the reduced rows then go through
+ * row band over as soon as that band's tiles are done).  Two spare warps of
+ * every GEMM CTA take 32 x 32 output blocks of the bands already complete and
+ * sum them while the GEMM still runs (the hand-over overlapped with the
+ * compute, as the pages overlap their scatter with it; not on the CTA-pair
+ * kernel, whose shared memory holds no room for it); band_reduce then waits
+ * (bounded) for each band's counter and sums the P partials of the remaining
+ * blocks in the same fixed order to bf16 out [M,N].  With GEMMAR_FP8_WIRE the reduced rows then go through
  * rowquant_e4m3 + rowdequant_e4m3 ("The fp8 wire").
  *   A[p], B[p], sa[p], sb[p]: HOST arrays of P device pointers; per slice as in
  *   gemm_blockscale_fp8 (scale_kind GEMMAR_SCALE_BLOCK128) or gemm_mxfp8

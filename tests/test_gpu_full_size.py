@@ -7,6 +7,7 @@ band plus random rows, all columns.
   - wo_b full chunk: the same at M = 8192 and M = 16384 (the headline shape)
   - fp8 wire on the M = 16384 output
   - mxfp8: P=4, A_p [16384, 2048], B_p [7168, 2048], ue8m0 1x32
+  - the band path's in-kernel reduce against GEMMAR_SERIAL_REDUCE, bitwise
 
 Operands are drawn by `synthetic` and quantised by the oracle on the host, so
 both sides consume identical codes and scales.  The M=4096 and M=8192 cases
@@ -120,6 +121,8 @@ def test_fused_mx_full_size(g):
                             [dev(s) for s in eb], out, scale_kind=g.GEMMAR_SCALE_MX32, bands=Pm)
         torch.cuda.synchronize()
         assert g.gemmar_status(ctx)[0] == 0
+        ov, tot = g.gemmar_overlap_stats(ctx)   # part of it summed while the GEMM ran
+        assert 0 < ov < tot, (ov, tot)
         rows = sample_rows(M, Pm, seed=5)
         got = out[torch.from_numpy(rows).cuda()].float().cpu().numpy()
         ref, _ = oracle.gemm_reduce(A, ea, B, eb, 1, rows=rows)
@@ -189,6 +192,9 @@ def test_fused_ptpc_full_size(g):
                                 [dev(s) for s in sb], out, scale_kind=g.GEMMAR_SCALE_PTPC, bands=P, flags=flags)
             torch.cuda.synchronize()
             assert g.gemmar_status(ctx)[0] == 0
+            if flags == 0:
+                ov, tot = g.gemmar_overlap_stats(ctx)   # part of it summed while the GEMM ran
+                assert 0 < ov < tot, (ov, tot)
             outs.append(out)
         assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
         rows = sample_rows(MMAX, P, seed=13)

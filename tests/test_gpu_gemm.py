@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import blockscale_operands, check_bf16_output, mx_operands, rel_l2
+from helpers import blockscale_operands, check_bf16_output, mx_operands, ptpc_operands, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -151,24 +151,26 @@ def test_fused_equals_split_bitwise_and_is_deterministic(g, ctx, kind):
     assert torch.equal(out1.view(torch.int16), split.view(torch.int16)), "fused != split"
 
 
-@pytest.mark.parametrize("P,M,N,K,bands", [(8, 1024, 1024, 512, 8), (3, 600, 768, 384, 3)])
-def test_band_path_overlap_equals_serial_reduce(g, ctx, P, M, N, K, bands):
+@pytest.mark.parametrize("kind", [0, 1, 2])
+@pytest.mark.parametrize("P,M,N,K,bands", [(8, 1024, 1024, 512, 8), (3, 600, 896, 384, 3)])
+def test_band_path_overlap_equals_serial_reduce(g, ctx, kind, P, M, N, K, bands):
     """The band path's in-kernel reduce (spare GEMM warps summing complete bands
     while the GEMM runs) against the same call with every block left to
     band_reduce: bit-equal, within the tolerance of the oracle, and the block
-    accounting consistent."""
-    A, sa, B, sb = blockscale_operands(P, M, N, K, seed=P + M)
-    over = run_fused(g, ctx, A, sa, B, sb, 0, bands, flags=g.GEMMAR_DEBUG_CANARY)
+    accounting consistent (blockscale, mx and ptpc kernels)."""
+    make = (blockscale_operands, mx_operands, ptpc_operands)[kind]
+    A, sa, B, sb = make(P, M, N, K, seed=P + M)
+    over = run_fused(g, ctx, A, sa, B, sb, kind, bands, flags=g.GEMMAR_DEBUG_CANARY)
     ov, tot = g.gemmar_overlap_stats(ctx)
-    rpb = M // bands
-    assert tot == bands * ((rpb + 127) // 128) * (N // 256 if N % 256 == 0 else N // 128) * 4 * (
-        8 if N % 256 == 0 else 4)
+    wide = 224 if kind == 1 else 256
+    bn = wide if N % wide == 0 else 128
+    assert tot == bands * ((M // bands + 127) // 128) * (N // bn) * 4 * (bn // 32)
     assert 0 <= ov <= tot
-    serial = run_fused(g, ctx, A, sa, B, sb, 0, bands, flags=g.GEMMAR_SERIAL_REDUCE | g.GEMMAR_DEBUG_CANARY)
+    serial = run_fused(g, ctx, A, sa, B, sb, kind, bands, flags=g.GEMMAR_SERIAL_REDUCE | g.GEMMAR_DEBUG_CANARY)
     assert g.gemmar_overlap_stats(ctx) == (0, 0)
     assert torch.equal(over.view(torch.int16), serial.view(torch.int16))
-    ref, _ = oracle.gemm_reduce(A, sa, B, sb, 0)
-    check_bf16_output(over.float().cpu().numpy(), ref, f"overlapped band path P={P} M={M}")
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, kind)
+    check_bf16_output(over.float().cpu().numpy(), ref, f"overlapped band path kind={kind} P={P} M={M}")
 
 
 def test_fused_fp8_wire(g, ctx):
