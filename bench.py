@@ -606,8 +606,8 @@ def run_profile_case(args):
     """One warm-up and one measured call of a single configuration, for
     profilers (ncu -k ... -s 1 -c 1): the fused layer (blockscale or ptpc P=8,
     mx P=4, at M rows, with --flags), or the row codec alone on a [M, 7168]
-    bf16 matrix (--codec).  No timing is printed; the exit status is the device
-    status."""
+    bf16 matrix (--codec).  No timing is printed (only, for the fused layer, the
+    share of blocks reduced during the GEMM); the exit status is the device status."""
     import torch
     import block_scaled_fp8_gemm_gb300 as g
     dev = torch.device("cuda", 0)
@@ -633,6 +633,9 @@ def run_profile_case(args):
             g.fused_gemm_reduce(ctx, A, sa, B, sb, out, scale_kind=kind, bands=P, flags=args.flags)
     torch.cuda.synchronize()
     code, detail = g.gemmar_status(ctx)
+    if not args.codec:
+        ov, tot = g.gemmar_overlap_stats(ctx)
+        print(f"blocks reduced during the GEMM: {ov} of {tot}", flush=True)
     ctx.close()
     return 0 if code == 0 else 1
 
@@ -645,7 +648,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle leg")
     ap.add_argument("--profile-case", action="store_true",
-                    help="single-shot case for profilers (see --kind, --m, --flags, --codec); prints nothing")
+                    help="single-shot case for profilers (see --kind, --m, --flags, --codec)")
     ap.add_argument("--kind", choices=("blockscale", "mx", "ptpc"), default="blockscale")
     ap.add_argument("--m", type=int, default=2048)
     ap.add_argument("--flags", type=int, default=0, help="fused_gemm_reduce flags (1 fp8 wire, 16 slice loop)")
