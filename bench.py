@@ -392,6 +392,20 @@ def run_ours(args, rank, world, local_rank):
     q_ms = wph["quantize"] / max(wcalls, 1)
     dq_ms = wph["dequantize"] / max(wcalls, 1)
     extra["fp8_wire_layer_us"] = wire_ms * 1e3
+    # the same wire with the row quantiser folded into the band reduce
+    step_wq = lambda: g.fused_gemm_reduce(ctx, A, sa, B, sb, out, bands=P,
+                                          flags=g.GEMMAR_FP8_WIRE | g.GEMMAR_FUSE_QUANTIZE)
+    for _ in range(2):
+        step_wq()
+    g.gemmar_set_phase_timing(ctx, True)
+    wq_ms = time_steps(step_wq, max(5, args.steps // 4), stream)
+    g.gemmar_set_phase_timing(ctx, False)
+    qph, qcalls = g.gemmar_phase_times(ctx)
+    extra["fp8_wire_fused_quantize"] = {
+        "us_per_layer": wq_ms * 1e3,
+        "phases_us": {k: v / max(qcalls, 1) * 1e3 for k, v in qph.items()},
+        "note": "GEMMAR_FUSE_QUANTIZE: the band reduce after the GEMM codes each row itself (no bf16 "
+                "write and re-read of the reduced rows); same output bits as fp8_wire_layer"}
     extra["rowquant"] = {"us": q_ms * 1e3, "GB/s": codec_bytes / (q_ms * 1e-3) / 1e9,
                          "frac_of_measured_hbm": codec_bytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
     extra["rowdequant"] = {"us": dq_ms * 1e3, "GB/s": codec_bytes / (dq_ms * 1e-3) / 1e9,

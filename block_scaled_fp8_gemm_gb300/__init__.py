@@ -55,6 +55,7 @@ GEMMAR_FUSE_SLICES = 1 << 4
 GEMMAR_CTA_PAIR = 1 << 5
 GEMMAR_FUSE_ONCHIP = 1 << 6
 GEMMAR_SERIAL_REDUCE = 1 << 7
+GEMMAR_FUSE_QUANTIZE = 1 << 8
 GEMMAR_MAX_P = 8
 GEMMAR_NOALLOC_MAX_PARTIALS = 8 * 1024 * 1024
 

@@ -486,6 +486,9 @@ GEMMAR_API int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A
     cudaStream_t st = as_stream(stream);
     ctx->ov_bands = 0;
     ctx->ov_total = 0;
+    // fp8 wire on the band path: the band reduce can quantise the rows itself
+    const bool fuse_q = !slices && (flags & GEMMAR_FP8_WIRE) && (flags & GEMMAR_FUSE_QUANTIZE) &&
+                        N <= kBandQuantMaxN;
     if (slices) {
         // every tile accumulates all P slices itself: no partials, no band reduce
         if (flags & GEMMAR_DEBUG_CANARY)
@@ -530,12 +533,19 @@ GEMMAR_API int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A
         if ((rc = run_gemm(ctx, P, A, sa, B, sb, scale_kind, M, N, K, bands, o, st)))
             return rc;
         mark(ctx, GEMMAR_PHASE_REDUCE, st);
-        CUDA_OK(launch_band_reduce_blocked(ctx->W, out, P, M, N, bands, bn, ctx->band_done, expected,
-                                           inkernel ? claim : nullptr, ctx->status, ctx->timeout_ns,
-                                           ctx->num_sms * 8, st));
+        if (fuse_q) {
+            // the remaining blocks' sums go straight to the row quantiser
+            CUDA_OK(launch_band_reduce_quant(ctx->W, out, P, M, N, bands, bn, ctx->band_done, expected,
+                                             inkernel ? claim : nullptr, ctx->wire_q, ctx->wire_s, ctx->status,
+                                             ctx->timeout_ns, st));
+        } else {
+            CUDA_OK(launch_band_reduce_blocked(ctx->W, out, P, M, N, bands, bn, ctx->band_done, expected,
+                                               inkernel ? claim : nullptr, ctx->status, ctx->timeout_ns,
+                                               ctx->num_sms * 8, st));
+        }
     }
     mark(ctx, GEMMAR_PHASE_QUANTIZE, st);
-    if (flags & GEMMAR_FP8_WIRE)
+    if ((flags & GEMMAR_FP8_WIRE) && !fuse_q)
         CUDA_OK(launch_rowquant(out, 1, M, N, ctx->wire_q, ctx->wire_s, ctx->num_sms, st));
     mark(ctx, GEMMAR_PHASE_DEQUANTIZE, st);
     if (flags & GEMMAR_FP8_WIRE)

@@ -115,6 +115,14 @@ cudaError_t launch_band_reduce(const float *W, uint16_t *out, int P, int64_t M, 
 // The same reduce over the fused path's tile-blocked partials (layout: epilogue.cuh).
 // claimed (device, [bands], may be nullptr): in band b the blocks below claimed[b]
 // were already reduced by the GEMM kernel's reducer warps (GemmOut::reduce_next).
+// The band reduce with the row quantiser folded in (fp8 wire): codes q [M, N] and
+// row scales s [M] from the blocked partials, taking the bf16 sums of the blocks
+// below claimed[b] (may be nullptr) from `out`.  N <= kBandQuantMaxN.
+constexpr int kBandQuantMaxN = 12288;   // 8 bf16 rows of N parked in shared memory
+cudaError_t launch_band_reduce_quant(const float *W, const uint16_t *out, int P, int64_t M, int64_t N, int bands,
+                                     int bn, const uint32_t *band_done, uint32_t expected, const uint32_t *claimed,
+                                     uint8_t *q, float *s, ptx::DevStatus *status, uint64_t timeout_ns,
+                                     cudaStream_t st);
 cudaError_t launch_band_reduce_blocked(const float *W, uint16_t *out, int P, int64_t M, int64_t N, int bands,
                                        int bn, const uint32_t *band_done, uint32_t expected,
                                        const uint32_t *claimed, ptx::DevStatus *status,

@@ -239,6 +239,8 @@ struct Enc {
         y = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
         fast = sc >= 0x1p-125f;   // 1/s < 2^125: finite, and q*(1+2^-21) cannot overflow
     }
+    // from the fields of an encoder built earlier (kept in shared memory)
+    __device__ __forceinline__ Enc(float sc, float y_, bool fast_) : s(sc), y(y_), fast(fast_) {}
     __device__ __forceinline__ uint32_t operator()(float a, float b, float c, float d) const
     {
         if (!fast)
@@ -331,6 +333,139 @@ __global__ void __launch_bounds__(256, 8) rowquant_bf16_cta_kernel(const uint16_
         o.x = enc(bf16_lo(w[c].x), bf16_hi(w[c].x), bf16_lo(w[c].y), bf16_hi(w[c].y));
         o.y = enc(bf16_lo(w[c].z), bf16_hi(w[c].z), bf16_lo(w[c].w), bf16_hi(w[c].w));
         __stcs(qr + t + c * T, o);
+    }
+}
+
+// --------------------------------------------------------------------------
+// Band reduce with the row quantiser folded in (the fp8 wire without the bf16
+// round trip): one CTA per 8 consecutive rows of a 32-row lane group of a band's
+// tile row.  Phase 1 forms each element of those rows exactly as the band
+// reduce does -- ((W_0 + W_1) + ...) in fp32, rounded to bf16 -- or, for the
+// 32 x 32 blocks the GEMM kernel's reducer warps already summed (block index
+// below claimed[b]), reads their bf16 result from `out`; it parks the 8 bf16
+// rows in shared memory and takes each row's amax on the way.  Phase 2 codes
+// the parked rows exactly as rowquant_bf16_cta_kernel does: s = amax / 448
+// (IEEE), codes = e4m3_rn_sat(x / s).  Loads: a warp covers 8 rows x 4 column
+// units of one chunk, four 128-byte pieces per slice.  The thread's row
+// (t & 7) is fixed, so its amax is one register.
+// --------------------------------------------------------------------------
+constexpr int kRqRows = 8;
+constexpr int kRqThreads = 512;
+
+template <int P>
+__global__ void __launch_bounds__(kRqThreads, 2) band_reduce_quant_kernel(
+    const float4 *__restrict__ W, const uint16_t *out, int N, int bands, int rows_per_band, int mt_per_band,
+    int ntiles_n, int bn, const uint32_t *band_done, uint32_t expected, const uint32_t *claimed,
+    uint8_t *__restrict__ q, float *__restrict__ s, DevStatus *status, uint64_t timeout_ns)
+{
+    extern __shared__ __align__(16) uint8_t rq_smem[];
+    uint16_t *park = reinterpret_cast<uint16_t *>(rq_smem);   // [kRqRows][N] bf16
+    __shared__ float red[kRqThreads / 32][kRqRows];
+    __shared__ float enc_s[kRqRows], enc_y[kRqRows];
+    __shared__ int enc_fast[kRqRows];
+    __shared__ int band_ok;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    // CTA -> (band, tile row, lane quarter, 8-row group)
+    int rest = blockIdx.x;
+    const int g8 = rest & 3;
+    rest >>= 2;
+    const int qq = rest & 3;
+    rest >>= 2;
+    const int mt = rest % mt_per_band;
+    const int b = rest / mt_per_band;
+    const int row0 = mt * 128 + qq * 32 + g8 * kRqRows;   // first row within the band
+    if (row0 >= rows_per_band)
+        return;
+    if (band_done != nullptr) {
+        if (t == 0) {
+            int ok = 1;
+            if (ld_acquire(band_done + b) < expected) {
+                const uint64_t t0 = globaltimer();
+                while (ld_acquire(band_done + b) < expected) {
+                    if (*(volatile int *)&status->code != 0) { ok = 0; break; }
+                    if (globaltimer() - t0 > timeout_ns) {
+                        report(status, kErrTimeout, SITE_REDUCE_BAND);
+                        ok = 0;
+                        break;
+                    }
+                    __nanosleep(256);
+                }
+            }
+            band_ok = ok;
+        }
+        __syncthreads();
+        if (!band_ok)
+            return;
+    }
+    const int nchunk = bn / 32;
+    const int64_t tiles_per_band = (int64_t)mt_per_band * ntiles_n;
+    const int64_t tile_f4 = 128 * (int64_t)bn / 4;
+    const int64_t slice_f4 = tiles_per_band * tile_f4;
+    const int64_t done = claimed != nullptr ? (int64_t)claimed[b] : 0;
+    const int r = t & (kRqRows - 1);
+    const bool row_ok = row0 + r < rows_per_band;
+    const int64_t m = (int64_t)b * rows_per_band + row0 + r;
+    const float4 *Wt = W + (int64_t)b * P * slice_f4 + qq * (nchunk * 8 * 32) + g8 * kRqRows + r;
+    float amax = 0.0f;
+    // phase 1: column quad cq of row r; a thread keeps r, steps cq by 32
+    for (int cq = t >> 3; cq < N / 4; cq += kRqThreads / kRqRows) {
+        const int col = cq * 4;
+        const int nt = col / bn, cin = col - nt * bn;
+        const int c = cin >> 5, u = (cin & 31) >> 2;
+        uint2 v = make_uint2(0u, 0u);
+        if (row_ok) {
+            const int64_t tile = (int64_t)mt * ntiles_n + nt;
+            const int64_t blk = (tile * 4 + qq) * nchunk + c;
+            if (blk < done) {
+                v = *reinterpret_cast<const uint2 *>(out + m * N + col);
+            } else {
+                const float4 *src = Wt + tile * tile_f4 + (c * 8 + u) * 32;
+                float4 w[P];
+#pragma unroll
+                for (int p = 0; p < P; ++p)
+                    w[p] = __ldcs(src + p * slice_f4);
+                float4 a = w[0];
+#pragma unroll
+                for (int p = 1; p < P; ++p) {
+                    a.x = a.x + w[p].x; a.y = a.y + w[p].y; a.z = a.z + w[p].z; a.w = a.w + w[p].w;
+                }
+                v = make_uint2(bf16x2_from_f32(a.x, a.y), bf16x2_from_f32(a.z, a.w));
+            }
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(v.x)), fabsf(bf16_hi(v.x))),
+                                     fmaxf(fabsf(bf16_lo(v.y)), fabsf(bf16_hi(v.y)))));
+        }
+        *reinterpret_cast<uint2 *>(park + r * N + col) = v;
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 8));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 16));
+    if (lane < kRqRows)
+        red[warp][lane] = amax;
+    __syncthreads();
+    if (t < kRqRows) {
+        float a = red[0][t];
+        for (int w = 1; w < kRqThreads / 32; ++w)
+            a = fmaxf(a, red[w][t]);
+        const float sc = __fdiv_rn(a, 448.0f);
+        const Enc e(sc);
+        enc_s[t] = e.s;
+        enc_y[t] = e.y;
+        enc_fast[t] = e.fast ? 1 : 0;
+        if (row0 + t < rows_per_band)
+            s[(int64_t)b * rows_per_band + row0 + t] = sc;
+    }
+    __syncthreads();
+    // phase 2: 8 elements per item, row-major over the parked rows
+    const int per_row = N / 8;
+    for (int i = t; i < kRqRows * per_row; i += kRqThreads) {
+        const int rr = i / per_row, g = i - rr * per_row;
+        if (row0 + rr >= rows_per_band)
+            break;   // rows past the band end come last
+        const Enc e(enc_s[rr], enc_y[rr], enc_fast[rr] != 0);
+        const uint4 w = *reinterpret_cast<const uint4 *>(park + rr * N + g * 8);
+        uint2 o;
+        o.x = e(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+        o.y = e(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+        __stcs(reinterpret_cast<uint2 *>(q + ((int64_t)b * rows_per_band + row0 + rr) * N) + g, o);
     }
 }
 
@@ -598,6 +733,41 @@ cudaError_t launch_rowquant(const void *x, int x_is_bf16, int64_t M, int64_t N, 
         rowquant_kernel<true><<<grid, 256, 0, st>>>(x, M, N, q, s);
     else
         rowquant_kernel<false><<<grid, 256, 0, st>>>(x, M, N, q, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_band_reduce_quant(const float *W, const uint16_t *out, int P, int64_t M, int64_t N, int bands,
+                                     int bn, const uint32_t *band_done, uint32_t expected, const uint32_t *claimed,
+                                     uint8_t *q, float *s, DevStatus *status, uint64_t timeout_ns, cudaStream_t st)
+{
+    if (N > kBandQuantMaxN || N % bn != 0 || bn % 32 != 0)
+        return cudaErrorInvalidValue;
+    const int rpb = (int)(M / bands), mtpb = (rpb + 127) / 128, ntn = (int)(N / bn);
+    const float4 *w4 = reinterpret_cast<const float4 *>(W);
+    const size_t smem = (size_t)kRqRows * N * 2;
+    const unsigned grid = (unsigned)bands * mtpb * 16;
+#define GEMMAR_RQ_CASE(PP)                                                                                     \
+    case PP: {                                                                                                 \
+        static bool configured = false;                                                                        \
+        if (!configured) {                                                                                     \
+            const cudaError_t e = cudaFuncSetAttribute(band_reduce_quant_kernel<PP>,                           \
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,            \
+                                                       (int)(kRqRows * kBandQuantMaxN * 2));                   \
+            if (e != cudaSuccess)                                                                              \
+                return e;                                                                                      \
+            configured = true;                                                                                 \
+        }                                                                                                      \
+        band_reduce_quant_kernel<PP><<<grid, kRqThreads, smem, st>>>(w4, out, (int)N, bands, rpb, mtpb, ntn, bn, \
+                                                                     band_done, expected, claimed, q, s, status, \
+                                                                     timeout_ns);                              \
+        break;                                                                                                 \
+    }
+    switch (P) {
+        GEMMAR_RQ_CASE(1) GEMMAR_RQ_CASE(2) GEMMAR_RQ_CASE(3) GEMMAR_RQ_CASE(4)
+        GEMMAR_RQ_CASE(5) GEMMAR_RQ_CASE(6) GEMMAR_RQ_CASE(7) GEMMAR_RQ_CASE(8)
+        default: return cudaErrorInvalidValue;
+    }
+#undef GEMMAR_RQ_CASE
     return cudaGetLastError();
 }
 

@@ -95,6 +95,9 @@ enum { GEMMAR_SCALE_BLOCK128 = 0, GEMMAR_SCALE_MX32 = 1, GEMMAR_SCALE_PTPC = 2 }
                                              fused_gemm_reduce */
 #define GEMMAR_SERIAL_REDUCE   (1u << 7)  /* fused band path: the GEMM kernel reduces no band while it
                                              runs; band_reduce sums every block after it (same bits) */
+#define GEMMAR_FUSE_QUANTIZE   (1u << 8)  /* fused band path with GEMMAR_FP8_WIRE, N <= 12288: the band
+                                             reduce quantises each row itself, without writing and
+                                             re-reading the bf16 rows (same bits); ignored otherwise */
 
 /* Largest number of K-slices ("ranks") one call takes. */
 #define GEMMAR_MAX_P 8
@@ -280,8 +283,14 @@ int quant_mx_e4m3(gemmar_ctx *ctx, const float *x, int64_t R, int64_t C, uint8_t
  * compute, as the pages overlap their scatter with it; not on the CTA-pair
  * kernel, whose shared memory holds no room for it); band_reduce then waits
  * (bounded) for each band's counter and sums the P partials of the remaining
- * blocks in the same fixed order to bf16 out [M,N].  With GEMMAR_FP8_WIRE the reduced rows then go through
- * rowquant_e4m3 + rowdequant_e4m3 ("The fp8 wire").
+ * blocks in the same fixed order to bf16 out [M,N].  With GEMMAR_FP8_WIRE the
+ * reduced rows then go through rowquant_e4m3 + rowdequant_e4m3 ("The fp8
+ * wire"); with GEMMAR_FUSE_QUANTIZE as well (N <= 12288), the band reduce
+ * parks each group of 8 summed bf16 rows in shared memory, takes their amax
+ * and writes their codes and scales itself (MORI page, "Negative results":
+ * folding the narrowing into the reduce), so the rows it sums are neither
+ * written as bf16 nor read back before rowdequant_e4m3; the output is
+ * bit-equal to the unfolded wire.
  *   A[p], B[p], sa[p], sb[p]: HOST arrays of P device pointers; per slice as in
  *   gemm_blockscale_fp8 (scale_kind GEMMAR_SCALE_BLOCK128) or gemm_mxfp8
  *   (GEMMAR_SCALE_MX32).  bands: row bands (0 = P).  out: bf16 [M,N].

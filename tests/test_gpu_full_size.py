@@ -107,6 +107,9 @@ def test_fp8_wire_full_size(g, headline):
     wire_ref = oracle.bf16_to_f32(oracle.rowdequant(q, s))
     assert rel_l2(got, ref) <= 3e-2
     assert rel_l2(got, wire_ref) <= 1e-2
+    # the band reduce quantising the rows itself gives the same bits
+    fused = run_fused(g, headline, M, flags=g.GEMMAR_FP8_WIRE | g.GEMMAR_FUSE_QUANTIZE)
+    assert torch.equal(fused.view(torch.int16), wire.view(torch.int16))
 
 
 def test_fused_mx_full_size(g):

@@ -195,6 +195,25 @@ def test_fused_fp8_wire(g, ctx):
     assert torch.equal(y.view(torch.int16), wire.view(torch.int16))
 
 
+@pytest.mark.parametrize("serial", [False, True])
+@pytest.mark.parametrize("kind", [0, 1, 2])
+@pytest.mark.parametrize("P,M,N,K,bands", [(8, 1024, 1024, 512, 8), (3, 600, 896, 384, 3), (2, 256, 512, 256, 2)])
+def test_fused_quantize_wire_equals_unfused_wire(g, ctx, kind, P, M, N, K, bands, serial):
+    """GEMMAR_FUSE_QUANTIZE (the band reduce codes each group of 8 summed rows
+    itself, taking the bf16 sums of blocks the GEMM kernel already reduced from
+    the output) against the unfolded fp8 wire: bit-equal, with and without the
+    in-kernel reduce, ragged bands included; and within the wire tolerance of
+    the oracle."""
+    make = (blockscale_operands, mx_operands, ptpc_operands)[kind]
+    A, sa, B, sb = make(P, M, N, K, seed=3 * P + M)
+    base = g.GEMMAR_FP8_WIRE | g.GEMMAR_DEBUG_CANARY | (g.GEMMAR_SERIAL_REDUCE if serial else 0)
+    plain = run_fused(g, ctx, A, sa, B, sb, kind, bands, flags=base)
+    fused = run_fused(g, ctx, A, sa, B, sb, kind, bands, flags=base | g.GEMMAR_FUSE_QUANTIZE)
+    assert torch.equal(fused.view(torch.int16), plain.view(torch.int16))
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, kind)
+    assert rel_l2(fused.float().cpu().numpy(), ref) <= 3e-2
+
+
 @pytest.mark.parametrize("kind,P,M,N,K", [(0, 2, 256, 512, 256), (0, 3, 600, 384, 384), (0, 8, 512, 256, 128),
                                           (1, 2, 256, 448, 256), (1, 3, 300, 256, 256)])
 def test_fused_slice_loop_vs_oracle_and_deterministic(g, ctx, kind, P, M, N, K):
