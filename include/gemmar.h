@@ -338,9 +338,11 @@ int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A, const voi
  * takes no context and allocates nothing (no cudaMalloc, no cudaFree, no
  * allocating library routine): its scratch -- fp32 partials for up to
  * GEMMAR_NOALLOC_MAX_PARTIALS elements (P*M*N, each band's rows rounded up to
- * whole 128-row tiles), 1024 band counters and a status word -- lives in fixed-size arrays in the library's device code,
- * which the CUDA driver reserves on every GPU that loads the library (32 MiB
- * plus a few KiB per GPU) and keeps until the process exits.
+ * whole 128-row tiles), 1024 band counters, 1024 claim counters for the
+ * GEMM's in-kernel band reduce and a status word -- lives in fixed-size arrays
+ * in the library's device code, which the CUDA driver reserves on every GPU
+ * that loads the library (32 MiB plus a few KiB per GPU) and keeps until the
+ * process exits.
  *
  * Arguments as fused_gemm_reduce with scale_kind GEMMAR_SCALE_BLOCK128 and no
  * flags: A, sa, B, sb are HOST arrays of P device pointers, out is bf16 [M,N]
