@@ -157,7 +157,7 @@ struct BandSignals {
 };
 
 // ---------------------------------------------------------------------------
-// In-kernel band reduce: one warp of a GEMM CTA sums retired bands while the
+// In-kernel band reduce: two warps of a GEMM CTA sum retired bands while the
 // CTA's other warps keep computing tiles.  It works on 32-row x 32-column
 // blocks of the blocked partials (numbered within a band as in
 // band_reduce_blocked_kernel: column chunk fastest, then lane quarter, then
@@ -166,14 +166,15 @@ struct BandSignals {
 // other CTAs have still to write: while the next band is incomplete it polls,
 // and it leaves as soon as its own CTA's epilogue warps are done (the band
 // reduce kernel launched after the GEMM takes, in every band, the blocks from
-// the final counter value on).  A block is read in four quarters (two 16-byte
-// column units of each lane's row, all P slices) through a four-stage cp.async
-// ring in shared memory; each lane loads and sums only its own row, so the ring
-// needs no warp barrier.  The arithmetic is that of the band reduce:
+// the final counter value on).  A block is read in eight items (one 16-byte
+// column unit of each lane's row, all P slices) through a four-stage cp.async
+// ring in shared memory per warp; each lane loads and sums only its own row, so
+// the ring needs no warp barrier.  The arithmetic is that of the band reduce:
 // ((W_0 + W_1) + W_2) + ..., fp32, then bf16 RN.
 // ---------------------------------------------------------------------------
 constexpr int kReduceRingStages = 4;
-constexpr int kReduceRingBytes = kReduceRingStages * 8 * 1024;   // at two units per item, P <= 8
+constexpr int kReduceWarpRingBytes = kReduceRingStages * kMaxP * 512;   // per reducer warp
+constexpr int kReduceRingBytes = 2 * kReduceWarpRingBytes;              // two reducer warps per CTA
 
 struct BandClaim {
     int band = 0;                // lowest band that may still have unclaimed blocks
@@ -226,16 +227,15 @@ __device__ __forceinline__ int claim_retired_block(const GemmOut &o, const TileG
     return __shfl_sync(0xffffffffu, blk, 0);
 }
 
-// UNITS: 16-byte column units of each lane's row per item (2: a block is four
-// items of P x 1 KB; 1: eight items of P x 512 B).  ring: shared address of
-// kReduceRingStages * UNITS * 4 KB (16-byte aligned) that nothing else uses while
-// the reducer runs.  Whole warp calls.
-template <int UNITS>
+// ring: shared address of kReduceWarpRingBytes (16-byte aligned) that nothing
+// else uses while this reducer warp runs.  A block is read as eight items, one
+// 16-byte column unit (4 columns) of each lane's row from every slice (P x 512 B
+// per item, one ring stage).  Whole warp calls.
 __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGrid &g, int bn, uint32_t ring,
                                                   const volatile int *epi_done, int epi_warps, uint64_t timeout_ns)
 {
-    constexpr int IPB = 8 / UNITS;                      // items per block
-    constexpr int STAGE = kMaxP * UNITS * 512;          // bytes per ring stage
+    constexpr int IPB = 8;                     // items per block
+    constexpr int STAGE = kMaxP * 512;         // bytes per ring stage
     const int lane = threadIdx.x & 31;
     const int P = g.P;
     const int nchunk = bn / 32;
@@ -244,11 +244,11 @@ __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGr
     const int64_t tile_f4 = 128 * (int64_t)bn / 4;
     const int64_t slice_f4 = tiles_per_band * tile_f4;
     const float4 *W = reinterpret_cast<const float4 *>(o.out);
-    int blk_even = -1, blk_odd = -1;   // block of items IPB*j..IPB*j+IPB-1: blk_even for even j, blk_odd for odd
+    int blk_even = -1, blk_odd = -1;   // block of items 8j..8j+7: blk_even for even j, blk_odd for odd
     bool more = true;
     int issued = 0;
     BandClaim cl;
-    // item k = units (k % IPB) * UNITS .. +UNITS-1 of its block, in ring stage k % kReduceRingStages
+    // item k = column unit k % 8 of its block, in ring stage k % kReduceRingStages
     auto issue = [&](int k) {
         const int j = (k / IPB) & 1;
         if (more && k % IPB == 0) {
@@ -265,12 +265,10 @@ __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGr
             const int c = (int)(r % nchunk), q = (int)((r / nchunk) & 3);
             const int64_t i = r / (4 * nchunk);
             const float4 *src = W + ((int64_t)b * P * tiles_per_band + i) * tile_f4 +
-                                ((q * nchunk + c) * 8 + UNITS * (k % IPB)) * 32 + lane;
+                                ((q * nchunk + c) * 8 + k % IPB) * 32 + lane;
             const uint32_t dst = ring + (k % kReduceRingStages) * STAGE + lane * 16;
             for (int p = 0; p < P; ++p)
-#pragma unroll
-                for (int u = 0; u < UNITS; ++u)
-                    ptx::cp_async_cg16(dst + (p * UNITS + u) * 512, src + p * slice_f4 + u * 32);
+                ptx::cp_async_cg16(dst + p * 512, src + p * slice_f4);
             ++issued;
         }
         ptx::cp_async_commit();   // one group per item slot, empty past the last item
@@ -282,20 +280,13 @@ __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGr
     for (int k = 0; k < issued; ++k) {
         ptx::cp_async_wait<kReduceRingStages - 1>();   // this lane's copies of item k have landed
         const uint32_t st = ring + (k % kReduceRingStages) * STAGE + lane * 16;
-        float a[4 * UNITS];
-#pragma unroll
-        for (int u = 0; u < UNITS; ++u) {
-            const uint4 w = ptx::ld_shared_v4(st + u * 512);
-            a[4 * u + 0] = __uint_as_float(w.x); a[4 * u + 1] = __uint_as_float(w.y);
-            a[4 * u + 2] = __uint_as_float(w.z); a[4 * u + 3] = __uint_as_float(w.w);
+        const uint4 w = ptx::ld_shared_v4(st);
+        float a[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z), __uint_as_float(w.w)};
+        for (int p = 1; p < P; ++p) {
+            const uint4 v = ptx::ld_shared_v4(st + p * 512);
+            a[0] = a[0] + __uint_as_float(v.x); a[1] = a[1] + __uint_as_float(v.y);
+            a[2] = a[2] + __uint_as_float(v.z); a[3] = a[3] + __uint_as_float(v.w);
         }
-        for (int p = 1; p < P; ++p)
-#pragma unroll
-            for (int u = 0; u < UNITS; ++u) {
-                const uint4 v = ptx::ld_shared_v4(st + (p * UNITS + u) * 512);
-                a[4 * u + 0] = a[4 * u + 0] + __uint_as_float(v.x); a[4 * u + 1] = a[4 * u + 1] + __uint_as_float(v.y);
-                a[4 * u + 2] = a[4 * u + 2] + __uint_as_float(v.z); a[4 * u + 3] = a[4 * u + 3] + __uint_as_float(v.w);
-            }
         const uint32_t blk = (uint32_t)(((k / IPB) & 1) ? blk_odd : blk_even);
         const uint32_t b = blk / bpb, r = blk % bpb;
         const int c = (int)(r % nchunk), q = (int)((r / nchunk) & 3);
@@ -304,14 +295,9 @@ __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGr
         const int row = mt * 128 + q * 32 + lane;   // row within the band
         if (row < g.rows_per_band) {
             const int64_t m = (int64_t)b * g.rows_per_band + row;
-            const int64_t col = (int64_t)nt * bn + c * 32 + (k % IPB) * UNITS * 4;
-            if constexpr (UNITS == 2)
-                *reinterpret_cast<uint4 *>(o.red_out + m * g.N + col) =
-                    make_uint4(ptx::bf16x2_from_f32(a[0], a[1]), ptx::bf16x2_from_f32(a[2], a[3]),
-                               ptx::bf16x2_from_f32(a[4], a[5]), ptx::bf16x2_from_f32(a[6], a[7]));
-            else
-                *reinterpret_cast<uint2 *>(o.red_out + m * g.N + col) =
-                    make_uint2(ptx::bf16x2_from_f32(a[0], a[1]), ptx::bf16x2_from_f32(a[2], a[3]));
+            const int64_t col = (int64_t)nt * bn + c * 32 + (k % IPB) * 4;
+            *reinterpret_cast<uint2 *>(o.red_out + m * g.N + col) =
+                make_uint2(ptx::bf16x2_from_f32(a[0], a[1]), ptx::bf16x2_from_f32(a[2], a[3]));
         }
         issue(k + kReduceRingStages);   // reuses this item's stage: this lane has read it
     }

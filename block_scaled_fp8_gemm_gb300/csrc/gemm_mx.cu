@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       } else if (prm.o.out_mode == OUT_PARTIAL_F32 && prm.o.reduce_next != nullptr) {
             // ------------------------------------------------ band reducers (warps 2-3; the
             // staging is unused when the epilogue writes blocked partials): half of it each
-            band_reducer_warp<1>(prm.o, g, BN, smem_u32(smem + C::kOffStaging) + (warp - 2) * (kReduceRingBytes / 2),
+            band_reducer_warp(prm.o, g, BN, smem_u32(smem + C::kOffStaging) + (warp - 2) * kReduceWarpRingBytes,
                                  epi_done, C::kEpiWarps, prm.timeout_ns);
       }
     } else {
