@@ -73,13 +73,16 @@ __device__ __forceinline__ float4 ld_scales4(const float *p)
 }
 
 // Scale one 16-column group of a ptpc tile row in place: w = (sa * sb[n]) * acc,
-// both products rounded to fp32 (the blockscale promotion's order).
-__device__ __forceinline__ void ptpc_scale16(uint32_t *r, float sa, const float *sb)
+// both products rounded to fp32 (the blockscale promotion's order).  The warp
+// holds its 128 per-channel scales one float4 per lane (loaded before the
+// TMEM-full wait, so the load latency hides under it); the group's 16 scales
+// are lanes src0 .. src0+3, broadcast by shuffles.
+__device__ __forceinline__ void ptpc_scale16(uint32_t *r, float sa, const float4 &mine, int src0)
 {
 #pragma unroll
     for (int j4 = 0; j4 < 4; ++j4) {
-        const float4 b = ld_scales4(sb + 4 * j4);
-        const float bs[4] = {b.x, b.y, b.z, b.w};
+        const float bs[4] = {__shfl_sync(0xFFFFFFFFu, mine.x, src0 + j4), __shfl_sync(0xFFFFFFFFu, mine.y, src0 + j4),
+                             __shfl_sync(0xFFFFFFFFu, mine.z, src0 + j4), __shfl_sync(0xFFFFFFFFu, mine.w, src0 + j4)};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             r[j4 * 4 + j] = __float_as_uint(__fmul_rn(__fmul_rn(sa, bs[j]), __uint_as_float(r[j4 * 4 + j])));
@@ -265,7 +268,76 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
         uint32_t titer = 0;
         BandSignals signals;
-        if (exact) {
+        if (exact && BN % 128 == 0) {
+            // Each slice's fp32 partial arrives in a TMEM buffer of its own; the
+            // warp owns a contiguous half of the tile row (BN/2 columns), reads it
+            // with 64-column loads (the buffer goes back to the MMA after the last
+            // one), scales it (ptpc) and folds it into a running sum in the band
+            // reducer's order, run = W_0, then run = run + W_p; bf16(run) is stored
+            // once per tile.
+            constexpr int HALF = BN / 2;
+            constexpr int NL = HALF / 64;   // 64-column TMEM loads per slice
+            bool ok = true;
+            for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
+                const TileCoord tc = decode_tile<BN>(t, g);
+                const int64_t mrow = min(tc.m0 + q * 32 + lane, g.M - 1);
+                // -0 is the identity of IEEE addition (-0 + x == x for every x, +0 and -0
+                // included), so run = -0, then run += W_p for p = 0.. gives W_0 first
+                float run[HALF];
+#pragma unroll
+                for (int j = 0; j < HALF; ++j)
+                    run[j] = -0.0f;
+                for (int sl = 0; sl < g.P; ++sl) {
+                    const float sa_m = PT ? __ldg(prm.pa[sl] + mrow) : 0.0f;
+                    // lane l: the scales of columns 4l .. 4l+3 of the warp's half
+                    float4 sb_mine = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    if (PT && lane < HALF / 4)
+                        sb_mine = ld_scales4(prm.pb[sl] + tc.n0 + h * HALF + lane * 4);
+                    const uint32_t buf = titer & 1, tph = (titer >> 1) & 1;
+                    if (!mbar_wait(tfull + buf, tph, abort_flag, prm.status, prm.timeout_ns, SITE_EPI_TMEM_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < NL; ++c) {
+                        uint32_t r[64];
+                        tmem_ld_x64(lane_base + buf * BN + h * HALF + c * 64, r);
+                        tmem_wait_ld(r);
+                        if (c == NL - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0)
+                                mbar_arrive(tempty + buf);
+                        }
+                        if constexpr (PT) {
+#pragma unroll
+                            for (int g16 = 0; g16 < 4; ++g16)
+                                ptpc_scale16(r + g16 * 16, sa_m, sb_mine, c * 16 + g16 * 4);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 64; ++j)
+                            run[c * 64 + j] = __fadd_rn(run[c * 64 + j], __uint_as_float(r[j]));
+                    }
+                    ++titer;
+                }
+                if (!ok)
+                    break;
+                const int rows_valid = max(0, min(32, tc.valid_rows - q * 32));
+                char *base = tile_out_base(prm.o, g, tc, 2) + ((int64_t)q * 32 * g.N + h * HALF) * 2;
+#pragma unroll
+                for (int c = 0; c < HALF / 32; ++c) {
+                    uint4 v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float *a = &run[c * 32 + u * 8];
+                        v[u] = make_uint4(bf16x2_from_f32(a[0], a[1]), bf16x2_from_f32(a[2], a[3]),
+                                          bf16x2_from_f32(a[4], a[5]), bf16x2_from_f32(a[6], a[7]));
+                    }
+                    store_chunk<4>(staging, v, base + c * 64, (int64_t)g.N * 2, rows_valid);
+                }
+            }
+        } else if (exact) {
             // Each slice's fp32 partial arrives in a TMEM buffer of its own; the
             // warp folds its 16-column groups h, h+2, ... into a running sum in the
             // band reducer's order (run = W_0, then run = run + W_p) and stores
@@ -275,10 +347,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
             for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
                 const TileCoord tc = decode_tile<BN>(t, g);
                 const int64_t mrow = min(tc.m0 + q * 32 + lane, g.M - 1);
+                // -0 is the identity of IEEE addition (-0 + x == x for every x, +0 and -0
+                // included), so run = -0, then run += W_p for p = 0.. gives W_0 first
                 float run[NH * 16];
+#pragma unroll
+                for (int j = 0; j < NH * 16; ++j)
+                    run[j] = -0.0f;
                 for (int sl = 0; sl < g.P; ++sl) {
                     const float sa_m = PT ? __ldg(prm.pa[sl] + mrow) : 0.0f;
-                    const float *sb_sl = PT ? prm.pb[sl] + tc.n0 + h * 16 : nullptr;
+                    // lane l: the scales of columns 4(l&3) .. +3 of the warp's 16-column group l>>2
+                    float4 sb_mine = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    if (PT && (lane >> 2) < NH)
+                        sb_mine = ld_scales4(prm.pb[sl] + tc.n0 + (h + 2 * (lane >> 2)) * 16 + (lane & 3) * 4);
                     const uint32_t buf = titer & 1, tph = (titer >> 1) & 1;
                     if (!mbar_wait(tfull + buf, tph, abort_flag, prm.status, prm.timeout_ns, SITE_EPI_TMEM_FULL)) {
                         ok = false;
@@ -291,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                         tmem_ld_x16(lane_base + buf * BN + (h + 2 * i) * 16, r);
                         tmem_wait_ld(r);
                         if constexpr (PT)
-                            ptpc_scale16(r, sa_m, sb_sl + i * 32);
+                            ptpc_scale16(r, sa_m, sb_mine, i * 4);
                         if (i == NH - 1) {
                             tc_fence_before();
                             __syncwarp();
@@ -300,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                         }
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            run[i * 16 + j] = sl == 0 ? __uint_as_float(r[j]) : __fadd_rn(run[i * 16 + j], __uint_as_float(r[j]));
+                            run[i * 16 + j] = __fadd_rn(run[i * 16 + j], __uint_as_float(r[j]));
                     }
                     ++titer;
                 }
@@ -323,12 +403,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         }
         for (int t = blockIdx.x; t < g.num_tiles && !exact; t += gridDim.x) {
             const TileCoord tc = decode_tile<BN>(t, g);
+            const float sa_m = PT ? __ldg(prm.pa[tc.p] + min(tc.m0 + q * 32 + lane, g.M - 1)) : 0.0f;
+            // lane l: the scales of columns 4(l&7) .. +3 of the warp's 32-column chunk l>>3
+            float4 sb_mine = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (PT && (lane >> 3) < NCH / 2)
+                sb_mine = ld_scales4(prm.pb[tc.p] + tc.n0 + (h + 2 * (lane >> 3)) * 32 + (lane & 7) * 4);
             const uint32_t buf = titer & 1, tph = (titer >> 1) & 1;
             if (!mbar_wait(tfull + buf, tph, abort_flag, prm.status, prm.timeout_ns, SITE_EPI_TMEM_FULL))
                 break;
             tc_fence_after();
             const int rows_valid = max(0, min(32, tc.valid_rows - q * 32));
-            const float sa_m = PT ? __ldg(prm.pa[tc.p] + min(tc.m0 + q * 32 + lane, g.M - 1)) : 0.0f;
             const int esz = prm.o.out_mode == OUT_BF16 ? 2 : 4;
             char *base = tile_out_base(prm.o, g, tc, esz) + (int64_t)q * 32 * g.N * esz;
             for (int c = h; c < NCH; c += 2) {
@@ -336,8 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                 tmem_ld_x32(lane_base + buf * BN + c * 32, r);
                 tmem_wait_ld(r);
                 if constexpr (PT) {
-                    ptpc_scale16(r, sa_m, prm.pb[tc.p] + tc.n0 + c * 32);
-                    ptpc_scale16(r + 16, sa_m, prm.pb[tc.p] + tc.n0 + c * 32 + 16);
+                    ptpc_scale16(r, sa_m, sb_mine, ((c - h) >> 1) * 8);
+                    ptpc_scale16(r + 16, sa_m, sb_mine, ((c - h) >> 1) * 8 + 4);
                 }
                 if (c + 2 >= NCH) {
                     tc_fence_before();
