@@ -96,7 +96,23 @@ def test_binding_constants_match_the_header(lib):
         if hasattr(g, name):
             assert getattr(g, name) == value, (name, getattr(g, name), value)
     # every flag bit is distinct
-    flags = [v for n, v in consts.items() if n in ("GEMMAR_FP8_WIRE", "GEMMAR_DEBUG_CANARY", "GEMMAR_FAULT_SKIP_BAND",
-                                                   "GEMMAR_NO_SELF_TEST", "GEMMAR_FUSE_SLICES", "GEMMAR_CTA_PAIR",
-                                                   "GEMMAR_FUSE_ONCHIP")]
-    assert len(flags) == len(set(flags)) == 7
+    flag_names = ("GEMMAR_FP8_WIRE", "GEMMAR_DEBUG_CANARY", "GEMMAR_FAULT_SKIP_BAND", "GEMMAR_NO_SELF_TEST",
+                  "GEMMAR_FUSE_SLICES", "GEMMAR_CTA_PAIR", "GEMMAR_FUSE_ONCHIP", "GEMMAR_SERIAL_REDUCE",
+                  "GEMMAR_FUSE_QUANTIZE")
+    flags = [consts[n] for n in flag_names]
+    assert len(flags) == len(set(flags)) == len(flag_names)
+    assert all(f & (f - 1) == 0 for f in flags)   # one bit each
+
+
+def test_host_side_argument_errors(lib):
+    """Entry points that take a context refuse a null one before touching the GPU."""
+    ARG = 1
+    st = lib.gemmar_overlap_stats
+    st.restype = ctypes.c_int
+    st.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]
+    a, b = ctypes.c_int64(7), ctypes.c_int64(7)
+    assert st(None, ctypes.byref(a), ctypes.byref(b)) == ARG
+    ps = lib.gemmar_phase_times
+    ps.restype = ctypes.c_int
+    ps.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]
+    assert ps(None, None, None) == ARG
