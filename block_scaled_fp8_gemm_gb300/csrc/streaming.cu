@@ -291,8 +291,10 @@ __global__ void __launch_bounds__(256) rowquant_kernel(const void *__restrict__ 
 // registers, the CTA reduces the amax through shared memory, and the row is
 // read from HBM exactly once.  Many small CTAs per SM keep the loads of
 // several rows in flight while other rows divide: the 32-register bound lets
-// nine rows (126 KB) be resident per SM, which outweighs the few spill slots
-// it costs (68 us instead of 73 us for 16384 x 7168 on GB300).
+// nine rows (126 KB) be resident per SM.  The kernel is close to issue-bound,
+// so the amax is taken on packed pairs (64 us instead of 68 us for
+// 16384 x 7168 on GB300; a persistent variant that prefetched the next row
+// into shared memory ran 80 us).
 __global__ void __launch_bounds__(256, 8) rowquant_bf16_cta_kernel(const uint16_t *__restrict__ x, int64_t N,
                                                                  uint8_t *__restrict__ q, float *__restrict__ s)
 {
@@ -305,14 +307,17 @@ __global__ void __launch_bounds__(256, 8) rowquant_bf16_cta_kernel(const uint16_
 #pragma unroll
     for (int c = 0; c < 4; ++c)
         w[c] = __ldcs(xr + t + c * T);
-    float amax = 0.0f;
+    // amax on packed pairs: max.xorsign.abs.bf16x2 keeps the larger magnitude
+    // of each half exactly (its sign is a xor of the inputs', dropped below)
+    uint32_t m2 = 0u;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         const uint32_t u[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[j])), fabsf(bf16_hi(u[j]))));
+            asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(u[j]));
     }
+    float amax = fmaxf(fabsf(bf16_lo(m2)), fabsf(bf16_hi(m2)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
