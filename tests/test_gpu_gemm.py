@@ -112,7 +112,9 @@ def run_fused(g, ctx, A, sa, B, sb, kind, bands, flags=0):
                                            (4, 512, 768, 256, 4),
                                            (3, 600, 384, 384, 3),      # ragged bands (200 rows)
                                            (8, 1024, 256, 128, 8),
-                                           (2, 256, 512, 256, 1)])
+                                           (2, 256, 512, 256, 1),
+                                           (1, 384, 512, 256, 3),      # one slice: the reduce is a rounding
+                                           (5, 1000, 640, 256, 8)])    # ragged: 125-row bands, 5 slices
 def test_fused_blockscale_vs_oracle(g, ctx, P, M, N, K, bands):
     A, sa, B, sb = blockscale_operands(P, M, N, K, seed=P * M)
     ref, _ = oracle.gemm_reduce(A, sa, B, sb, 0)
