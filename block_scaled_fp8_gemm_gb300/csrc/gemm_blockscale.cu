@@ -311,14 +311,10 @@ template <int BN>
 cudaError_t launch_bn(const BsParams &p, int grid, cudaStream_t s)
 {
     using C = BsCfg<BN>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_blockscale_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::kSmemBytes);
-        if (e != cudaSuccess)
-            return e;
-        configured = true;
-    }
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(gemm_blockscale_kernel<BN>),
+                                              C::kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
     gemm_blockscale_kernel<BN><<<grid, kThreads, C::kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }

@@ -444,17 +444,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const 
         tmem_dealloc_pair(tmem_base, 512);
 }
 
-int max_clusters_cached = -1;
+constexpr int kMaxDevices = 64;
+int max_clusters_cached[kMaxDevices];   // per device: 0 unknown, else clusters + 1
 
 }  // namespace
 
 int gemm_blockscale_2sm_max_clusters()
 {
-    if (max_clusters_cached >= 0)
-        return max_clusters_cached;
-    if (cudaFuncSetAttribute(gemm_blockscale_2sm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-        cudaSuccess) {
-        max_clusters_cached = 0;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return 0;
+    if (max_clusters_cached[dev] > 0)
+        return max_clusters_cached[dev] - 1;
+    if (ensure_dynamic_smem(reinterpret_cast<const void *>(gemm_blockscale_2sm_kernel), kSmemBytes) != cudaSuccess) {
+        max_clusters_cached[dev] = 1;
         return 0;
     }
     cudaLaunchConfig_t cfg = {};
@@ -471,7 +474,7 @@ int gemm_blockscale_2sm_max_clusters()
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, gemm_blockscale_2sm_kernel, &cfg) != cudaSuccess)
         n = 0;
-    max_clusters_cached = n;
+    max_clusters_cached[dev] = n + 1;
     return n;
 }
 
@@ -531,6 +534,9 @@ cudaError_t launch_blockscale(const BsParams &p, const BsPlan &plan, cudaStream_
 
 cudaError_t launch_gemm_blockscale_2sm(const BsParams &p, int clusters, cudaStream_t s)
 {
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(gemm_blockscale_2sm_kernel), kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -472,14 +472,9 @@ template <int BN, bool PT>
 cudaError_t launch_bn(const MxParams &p, int grid, cudaStream_t s)
 {
     using C = MxCfg<BN, PT>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e =
-            cudaFuncSetAttribute(gemm_mx_kernel<BN, PT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-        if (e != cudaSuccess)
-            return e;
-        configured = true;
-    }
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(gemm_mx_kernel<BN, PT>), C::kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
     gemm_mx_kernel<BN, PT><<<grid, kThreads, C::kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }

@@ -9,6 +9,8 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <set>
+#include <utility>
 #include <vector>
 
 #include "gemmar.h"
@@ -46,6 +48,27 @@ struct gemmar_ctx {
     std::vector<cudaEvent_t> events;
     int recorded = 0;
 };
+
+namespace gemmar {
+
+cudaError_t ensure_dynamic_smem(const void *kernel, int bytes)
+{
+    static std::mutex mu;
+    static std::set<std::pair<const void *, int>> done;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({kernel, dev}))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        done.insert({kernel, dev});
+    return e;
+}
+
+}  // namespace gemmar
 
 namespace {
 

@@ -74,6 +74,11 @@ struct MxParams {
     uint64_t timeout_ns;
 };
 
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) for the current device, done
+// once per (kernel, device): the attribute belongs to the kernel's instance on
+// each device, so a process that drives several GPUs sets it on each.
+cudaError_t ensure_dynamic_smem(const void *kernel, int bytes);
+
 // GEMM launchers (bn: 256 or 128 for blockscale; 224 or 128 for mx).
 cudaError_t launch_gemm_blockscale(const BsParams &p, int bn, int grid, cudaStream_t s);
 cudaError_t launch_gemm_mx(const MxParams &p, int bn, int grid, cudaStream_t s);

@@ -753,15 +753,10 @@ cudaError_t launch_band_reduce_quant(const float *W, const uint16_t *out, int P,
     const unsigned grid = (unsigned)bands * mtpb * 16;
 #define GEMMAR_RQ_CASE(PP)                                                                                     \
     case PP: {                                                                                                 \
-        static bool configured = false;                                                                        \
-        if (!configured) {                                                                                     \
-            const cudaError_t e = cudaFuncSetAttribute(band_reduce_quant_kernel<PP>,                           \
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,            \
-                                                       (int)(kRqRows * kBandQuantMaxN * 2));                   \
-            if (e != cudaSuccess)                                                                              \
-                return e;                                                                                      \
-            configured = true;                                                                                 \
-        }                                                                                                      \
+        const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(band_reduce_quant_kernel<PP>), \
+                                                  (int)(kRqRows * kBandQuantMaxN * 2));                         \
+        if (e != cudaSuccess)                                                                                  \
+            return e;                                                                                          \
         band_reduce_quant_kernel<PP><<<grid, kRqThreads, smem, st>>>(w4, out, (int)N, bands, rpb, mtpb, ntn, bn, \
                                                                      band_done, expected, claimed, q, s, status, \
                                                                      timeout_ns);                              \
