@@ -158,7 +158,10 @@ int64_t gemmar_workspace_bytes(const gemmar_ctx *ctx);
  * recorded calls into ms[GEMMAR_NUM_PHASES] and the number of calls into
  * *calls, and clears the record.  Phases: GEMMAR_PHASE_GEMM (scale repack,
  * GEMM with band-ordered partial stores), GEMMAR_PHASE_REDUCE (band_reduce),
- * GEMMAR_PHASE_QUANTIZE and GEMMAR_PHASE_DEQUANTIZE (the fp8 wire; 0 when off).
+ * GEMMAR_PHASE_QUANTIZE and GEMMAR_PHASE_DEQUANTIZE (the fp8 wire; 0 when off;
+ * with GEMMAR_FUSE_QUANTIZE the quantiser runs inside GEMMAR_PHASE_REDUCE).  On
+ * the band path with the in-kernel reduce, GEMMAR_PHASE_GEMM includes the blocks
+ * the GEMM kernel summed (gemmar_overlap_stats) and GEMMAR_PHASE_REDUCE the rest.
  * At most 65536 calls are recorded between reads (later ones are not timed).
  */
 enum { GEMMAR_PHASE_GEMM = 0, GEMMAR_PHASE_REDUCE = 1, GEMMAR_PHASE_QUANTIZE = 2,
