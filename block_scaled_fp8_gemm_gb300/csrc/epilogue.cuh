@@ -245,6 +245,9 @@ __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGr
     const int64_t slice_f4 = tiles_per_band * tile_f4;
     const float4 *W = reinterpret_cast<const float4 *>(o.out);
     int blk_even = -1, blk_odd = -1;   // block of items 8j..8j+7: blk_even for even j, blk_odd for odd
+    // bf16 sums of the last four items: 16 columns of the lane's row
+    uint32_t o0 = 0, o1 = 0, o2 = 0, o3 = 0, o4 = 0, o5 = 0, o6 = 0, o7 = 0;
+    const bool out32 = (reinterpret_cast<uintptr_t>(o.red_out) & 31) == 0;
     bool more = true;
     int issued = 0;
     BandClaim cl;
@@ -292,12 +295,29 @@ __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGr
         const int c = (int)(r % nchunk), q = (int)((r / nchunk) & 3);
         const int64_t i = r / (4 * nchunk);
         const int mt = (int)(i / g.ntiles_n), nt = (int)(i % g.ntiles_n);
+        // four consecutive items are 16 consecutive columns of the lane's row: 32
+        // bytes, stored as one full sector once the fourth is summed
+        {
+            const uint32_t lo = ptx::bf16x2_from_f32(a[0], a[1]), hi = ptx::bf16x2_from_f32(a[2], a[3]);
+            const int slot = k & 3;   // registers, not an indexed array: selected moves
+            o0 = slot == 0 ? lo : o0; o1 = slot == 0 ? hi : o1;
+            o2 = slot == 1 ? lo : o2; o3 = slot == 1 ? hi : o3;
+            o4 = slot == 2 ? lo : o4; o5 = slot == 2 ? hi : o5;
+            o6 = slot == 3 ? lo : o6; o7 = slot == 3 ? hi : o7;
+        }
         const int row = mt * 128 + q * 32 + lane;   // row within the band
-        if (row < g.rows_per_band) {
+        if ((k & 3) == 3 && row < g.rows_per_band) {
             const int64_t m = (int64_t)b * g.rows_per_band + row;
-            const int64_t col = (int64_t)nt * bn + c * 32 + (k % IPB) * 4;
-            *reinterpret_cast<uint2 *>(o.red_out + m * g.N + col) =
-                make_uint2(ptx::bf16x2_from_f32(a[0], a[1]), ptx::bf16x2_from_f32(a[2], a[3]));
+            const int64_t col = (int64_t)nt * bn + c * 32 + ((k % IPB) & 4) * 4;
+            uint16_t *dst = o.red_out + m * g.N + col;
+            if (out32)   // rows are 32-byte multiples; the output base decides
+                asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(o0),
+                             "r"(o1), "r"(o2), "r"(o3), "r"(o4), "r"(o5), "r"(o6), "r"(o7)
+                             : "memory");
+            else {
+                reinterpret_cast<uint4 *>(dst)[0] = make_uint4(o0, o1, o2, o3);
+                reinterpret_cast<uint4 *>(dst)[1] = make_uint4(o4, o5, o6, o7);
+            }
         }
         issue(k + kReduceRingStages);   // reuses this item's stage: this lane has read it
     }

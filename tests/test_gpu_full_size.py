@@ -154,6 +154,16 @@ def test_band_path_overlap_full_size(g, headline, M):
     assert 0 < ov < tot, (ov, tot)
     serial = run_fused(g, headline, M, flags=g.GEMMAR_SERIAL_REDUCE)
     assert torch.equal(over.view(torch.int16), serial.view(torch.int16))
+    # an output base that is 16- but not 32-byte aligned takes the reducers' 16-byte stores
+    base = torch.empty(M * N + 8, dtype=torch.bfloat16, device="cuda")
+    shifted = base[8:].view(M, N)
+    assert shifted.data_ptr() % 32 == 16
+    g.fused_gemm_reduce(headline["ctx"], [a[:M] for a in headline["dA"]], [s[:M] for s in headline["dsa"]],
+                        headline["dB"], headline["dsb"], shifted, bands=P)
+    torch.cuda.synchronize()
+    assert g.gemmar_status(headline["ctx"])[0] == 0
+    assert g.gemmar_overlap_stats(headline["ctx"])[0] > 0
+    assert torch.equal(shifted.view(torch.int16), over.view(torch.int16))
 
 
 def test_onchip_full_size_bit_equal_to_pair_band_path(g, headline):
