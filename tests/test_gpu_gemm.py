@@ -170,6 +170,8 @@ def test_band_path_overlap_equals_serial_reduce(g, ctx, kind, P, M, N, K, bands)
     assert 0 <= ov <= tot
     serial = run_fused(g, ctx, A, sa, B, sb, kind, bands, flags=g.GEMMAR_SERIAL_REDUCE | g.GEMMAR_DEBUG_CANARY)
     assert g.gemmar_overlap_stats(ctx) == (0, 0)
+    run_fused(g, ctx, A, sa, B, sb, kind, bands, flags=g.GEMMAR_FUSE_SLICES)   # no band path: nothing to report
+    assert g.gemmar_overlap_stats(ctx) == (0, 0)
     assert torch.equal(over.view(torch.int16), serial.view(torch.int16))
     ref, _ = oracle.gemm_reduce(A, sa, B, sb, kind)
     check_bf16_output(over.float().cpu().numpy(), ref, f"overlapped band path kind={kind} P={P} M={M}")
