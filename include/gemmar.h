@@ -86,7 +86,8 @@ enum { GEMMAR_SCALE_BLOCK128 = 0, GEMMAR_SCALE_MX32 = 1, GEMMAR_SCALE_PTPC = 2 }
                                              kernel (256 x 256 tiles over two SMs, band partials parked in
                                              shared memory and sent by bulk async copies) instead of the
                                              one-CTA kernel; same results within tolerance; on the wo_b
-                                             band path about as fast */
+                                             band path slower (its GEMM ~2040 us against ~1780), and
+                                             without the in-kernel band reduce */
 #define GEMMAR_FUSE_SLICES     (1u << 4)  /* fused: each output tile accumulates all P slices itself (no
                                              partials, no band reduce); see fused_gemm_reduce */
 #define GEMMAR_FUSE_ONCHIP     (1u << 6)  /* fused: the P slice partials of a tile stay on chip and are
