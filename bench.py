@@ -421,7 +421,7 @@ def run_ours(args, rank, world, local_rank):
                                  "note": "GEMMAR_FUSE_SLICES: one fp32 chain per output over all slices"}
 
     # ---- the same layer with each tile's P slice partials summed on chip in the
-    # band reducer's order (bit-equal to the band path of the CTA-pair kernel)
+    # band reducer's order (bit-equal to the band path)
     step_oc = lambda: g.fused_gemm_reduce(ctx, A, sa, B, sb, out, bands=P, flags=g.GEMMAR_FUSE_ONCHIP)
     for _ in range(2):
         step_oc()
@@ -430,7 +430,7 @@ def run_ours(args, rank, world, local_rank):
                              "frac_of_fp8_peak": fl / (ms_oc * 1e-3) / 1e12 / fp8_peak,
                              "note": "GEMMAR_FUSE_ONCHIP: CTA-pair kernel, per-slice fp32 partials summed "
                                      "in shared memory in the reducer's order; output bit-equal to the "
-                                     "CTA-pair band path (tests), no partial traffic"}
+                                     "headline band path (tests), no partial traffic"}
 
     # ---- the same layer at M = 8192
     M2 = 8192

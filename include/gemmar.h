@@ -92,8 +92,7 @@ enum { GEMMAR_SCALE_BLOCK128 = 0, GEMMAR_SCALE_MX32 = 1, GEMMAR_SCALE_PTPC = 2 }
                                              partials, no band reduce); see fused_gemm_reduce */
 #define GEMMAR_FUSE_ONCHIP     (1u << 6)  /* fused: the P slice partials of a tile stay on chip and are
                                              summed in the band reducer's order; bit-equal to the band
-                                             path (blockscale: of a GEMMAR_CTA_PAIR context); see
-                                             fused_gemm_reduce */
+                                             path; see fused_gemm_reduce */
 #define GEMMAR_SERIAL_REDUCE   (1u << 7)  /* fused band path: the GEMM kernel reduces no band while it
                                              runs; band_reduce sums every block after it (same bits) */
 #define GEMMAR_FUSE_QUANTIZE   (1u << 8)  /* fused band path with GEMMAR_FP8_WIRE, N <= 12288: the band
@@ -316,7 +315,8 @@ int quant_mx_e4m3(gemmar_ctx *ctx, const float *x, int64_t R, int64_t C, uint8_t
  * W_1) + W_2) + ..., in fp32 before the single bf16 rounding, without the
  * 2 x P*M*N*4 bytes of partial traffic.  Blockscale (N % 256 == 0, a GPU that
  * runs CTA pairs) runs on the CTA-pair kernel, the running sum in shared
- * memory: bit-equal to the band path of a GEMMAR_CTA_PAIR context.  mx and
+ * memory: bit-equal to the band path, of the default one-CTA kernel as of a
+ * GEMMAR_CTA_PAIR context (the two kernels give the same bits).  mx and
  * ptpc run on the whole-K kernel, each slice accumulating in a TMEM buffer of
  * its own (ptpc: then scaled) and the running sum in registers: bit-equal to
  * their band path.  Other blockscale shapes take the band path.  Takes

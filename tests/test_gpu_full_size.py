@@ -168,8 +168,10 @@ def test_band_path_overlap_full_size(g, headline, M):
 
 def test_onchip_full_size_bit_equal_to_pair_band_path(g, headline):
     """GEMMAR_FUSE_ONCHIP at the headline shape: sampled rows against the oracle,
-    and the whole output bit-equal to the band path of the CTA-pair kernel."""
+    and the whole output bit-equal to the band path of the CTA-pair kernel and to
+    the default one-CTA band path (the benchmark's headline step)."""
     M = MMAX
+    band_one_cta = run_fused(g, headline, M)
     ctx2 = g.gemmar_create(0, M, N, K, P, flags=g.GEMMAR_CTA_PAIR)
     try:
         outs = []
@@ -181,6 +183,7 @@ def test_onchip_full_size_bit_equal_to_pair_band_path(g, headline):
             assert g.gemmar_status(ctx2)[0] == 0
             outs.append(out)
         assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+        assert torch.equal(outs[0].view(torch.int16), band_one_cta.view(torch.int16))
         rows = sample_rows(M, P, seed=11)
         got = outs[0][torch.from_numpy(rows).cuda()].float().cpu().numpy()
         ref, _ = oracle_rows(headline, M, rows)

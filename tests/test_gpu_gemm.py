@@ -250,10 +250,9 @@ def test_pair_and_single_cta_kernels_agree(g, ctx, ctx_pair, P, M, N, K, bands):
     one = run_fused(g, ctx, A, sa, B, sb, 0, bands, flags=g.GEMMAR_DEBUG_CANARY)
     check_bf16_output(pair.float().cpu().numpy(), ref, f"pair kernel P={P} M={M} N={N} K={K}")
     check_bf16_output(one.float().cpu().numpy(), ref, f"one-CTA kernel P={P} M={M} N={N} K={K}")
-    # the same fp32 promotion order on both: outputs differ by at most one bf16 ulp
-    a = pair.view(torch.int16).int()
-    b = one.view(torch.int16).int()
-    assert int((a - b).abs().max()) <= 1
+    # the same fp32 promotion order on both, and the tensor cores accumulate a
+    # K-block the same way for M=256 pairs as for M=128: the same bits
+    assert torch.equal(pair.view(torch.int16), one.view(torch.int16))
 
 
 @pytest.mark.parametrize("M,N,K", [(200, 384, 512), (1, 128, 128), (384, 768, 384)])
@@ -315,8 +314,8 @@ def test_onchip_on_default_context_matches_one_cta_band_path(g, ctx):
     onchip = run_fused(g, ctx, A, sa, B, sb, 0, P, flags=g.GEMMAR_FUSE_ONCHIP)
     band = run_fused(g, ctx, A, sa, B, sb, 0, P)
     check_bf16_output(onchip.float().cpu().numpy(), ref, "on-chip, default context")
-    d = (onchip.view(torch.int16).int() - band.view(torch.int16).int()).abs()
-    assert int(d.max()) <= 1
+    # the on-chip sums (CTA-pair kernel) reproduce the one-CTA band path's bits
+    assert torch.equal(onchip.view(torch.int16), band.view(torch.int16))
 
 
 # ------------------------------------------------------------ ptpc (per-token / per-channel scales)
