@@ -85,7 +85,7 @@ enum { GEMMAR_SCALE_BLOCK128 = 0, GEMMAR_SCALE_MX32 = 1, GEMMAR_SCALE_PTPC = 2 }
 #define GEMMAR_CTA_PAIR        (1u << 5)  /* create: run blockscale GEMMs with N % 256 == 0 on the CTA-pair
                                              kernel (256 x 256 tiles over two SMs, band partials parked in
                                              shared memory and sent by bulk async copies) instead of the
-                                             one-CTA kernel; same results within tolerance; on the wo_b
+                                             one-CTA kernel; the same bits (tests); on the wo_b
                                              band path slower (its GEMM ~2040 us against ~1780), and
                                              without the in-kernel band reduce */
 #define GEMMAR_FUSE_SLICES     (1u << 4)  /* fused: each output tile accumulates all P slices itself (no
