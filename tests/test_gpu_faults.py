@@ -55,9 +55,10 @@ def test_host_side_errors_launch_nothing(g):
     ctx.close()
 
 
-@pytest.mark.parametrize("kind,create_flags", [(0, 0), (0, "pair"), (1, 0), (2, 0)],
-                         ids=["blockscale", "blockscale-cta-pair", "mx", "ptpc"])
-def test_unsignalled_band_times_out_cleanly(g, kind, create_flags):
+@pytest.mark.parametrize("kind,create_flags,call_flags",
+                         [(0, 0, 0), (0, "pair", 0), (1, 0, 0), (2, 0, 0), (0, 0, "fuse_quantize")],
+                         ids=["blockscale", "blockscale-cta-pair", "mx", "ptpc", "blockscale-fused-quantize"])
+def test_unsignalled_band_times_out_cleanly(g, kind, create_flags, call_flags):
     from helpers import mx_operands, ptpc_operands
     torch.cuda.set_device(0)
     cflags = g.GEMMAR_NO_SELF_TEST | (g.GEMMAR_CTA_PAIR if create_flags == "pair" else 0)
@@ -66,7 +67,8 @@ def test_unsignalled_band_times_out_cleanly(g, kind, create_flags):
     A, sa, B, sb = make(2, 256, 512, 256, seed=2)
     dA, dsa, dB, dsb = [dev(a) for a in A], [dev(s) for s in sa], [dev(b) for b in B], [dev(s) for s in sb]
     out = torch.empty((256, 512), dtype=torch.bfloat16, device="cuda")
-    g.fused_gemm_reduce(ctx, dA, dsa, dB, dsb, out, scale_kind=kind, flags=g.GEMMAR_FAULT_SKIP_BAND)
+    extra = g.GEMMAR_FP8_WIRE | g.GEMMAR_FUSE_QUANTIZE if call_flags == "fuse_quantize" else 0
+    g.fused_gemm_reduce(ctx, dA, dsa, dB, dsb, out, scale_kind=kind, flags=g.GEMMAR_FAULT_SKIP_BAND | extra)
     torch.cuda.synchronize()                    # the wait gave up: no hang, context still usable
     code, detail = g.gemmar_status(ctx)
     assert code == g.GEMMAR_ERR_TIMEOUT and detail == 7      # the reducer's band wait
