@@ -59,3 +59,14 @@ def check_bf16_output(got, ref, what=""):
     assert rl <= REL_L2_MAX, f"{what}: relL2 {rl:.3e} > {REL_L2_MAX}"
     assert not bad.any(), f"{what}: {int(bad.sum())} elements out of bound, worst {err[bad].max():.3e}"
     return rl
+
+
+def check_f32_output(got, ref, what=""):
+    """An fp32 single-slice GEMM against fp64: fp32 accumulation and promotion
+    cost a few fp32 roundings of the magnitudes involved."""
+    got = np.asarray(got, np.float64)
+    scale = np.sqrt(np.mean(ref ** 2))
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)), what
+    assert rel_l2(got, ref) <= 2e-6, (what, rel_l2(got, ref))
+    assert np.all(err <= 1e-5 * np.abs(ref) + 2e-5 * scale), (what, err.max())

@@ -12,13 +12,18 @@ bit for bit:
   - the fp8 wire, with and without the row quantiser folded into the reduce,
     both equal to the library's row codec applied to the band path's rows.
 The draws include one-row bands, bands that end inside a tile, P = 1, and
-N on both mxfp8 tile widths (multiples of 128 and of 224)."""
+N on both mxfp8 tile widths (multiples of 128 and of 224).
+
+The single kernels get random shapes too: each scale kind's one-slice GEMM
+with an fp32 output against the oracle, and the band reduce and the row codec
+bit for bit against the oracle's fp32 ordered sum and row codec."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from helpers import blockscale_operands, check_bf16_output, mx_operands, ptpc_operands
+import synthetic
+from helpers import blockscale_operands, check_bf16_output, check_f32_output, mx_operands, ptpc_operands
 
 pytestmark = pytest.mark.gpu
 
@@ -118,3 +123,84 @@ def test_random_shape(g, ctx, ctx_pair, kind, P, M, N, K, bands):
     assert torch.equal(bits(wire), bits(y)), f"{what}: fp8 wire != codec of the band path"
     wire_q = fused(g.GEMMAR_FP8_WIRE | g.GEMMAR_FUSE_QUANTIZE)
     assert torch.equal(bits(wire_q), bits(y)), f"{what}: folded-quantiser wire != codec of the band path"
+
+
+def draw_gemm_shapes(kind, n, seed):
+    rng = np.random.RandomState(seed)
+    n_choices = [c for c in range(128, MAX_N + 1, 32) if c % 128 == 0 or (kind == 1 and c % 224 == 0)]
+    return [(int(rng.randint(1, MAX_M + 1)), int(rng.choice(n_choices)), int(rng.choice([128, 256, 384, 512])))
+            for _ in range(n)]
+
+
+GEMM_CASES = [(kind, *shape) for kind in (0, 1, 2) for shape in draw_gemm_shapes(kind, 6, 7200 + kind)]
+
+
+@pytest.mark.parametrize("kind,M,N,K", GEMM_CASES, ids=[f"k{k}-M{M}-N{N}-K{K}" for k, M, N, K in GEMM_CASES])
+def test_random_single_gemm(g, ctx, kind, M, N, K):
+    make = (blockscale_operands, mx_operands, ptpc_operands)[kind]
+    gemm = (g.gemm_blockscale_fp8, g.gemm_mxfp8, g.gemm_ptpc_fp8)[kind]
+    A, sa, B, sb = make(1, M, N, K, seed=M * 7 + N * 3 + K)
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    gemm(ctx, dev(A[0]), dev(sa[0]), dev(B[0]), dev(sb[0]), C)
+    torch.cuda.synchronize()
+    assert g.gemmar_status(ctx)[0] == 0
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, kind)
+    check_f32_output(C.cpu().numpy(), ref, f"kind {kind} {M}x{N}x{K}")
+
+
+def draw_reduce_shapes(n, seed):
+    rng = np.random.RandomState(seed)
+    out = []
+    for _ in range(n):
+        bands = int(rng.randint(1, 9))
+        out.append((int(rng.randint(1, MAX_P + 1)), bands * int(rng.randint(1, 300)),
+                    8 * int(rng.randint(1, 257)), bands))
+    return out
+
+
+REDUCE_CASES = draw_reduce_shapes(8, 7300)
+
+
+@pytest.mark.parametrize("P,M,N,bands", REDUCE_CASES, ids=[f"P{P}-M{M}-N{N}-b{b}" for P, M, N, b in REDUCE_CASES])
+def test_random_band_reduce(g, ctx, P, M, N, bands):
+    rpb = M // bands
+    W = synthetic.normal(P + M + N, synthetic.TID_W, P, (bands, P, rpb, N))
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    g.band_reduce(ctx, dev(W), P, M, N, bands, out)
+    torch.cuda.synchronize()
+    assert g.gemmar_status(ctx)[0] == 0
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    for b in range(bands):
+        assert np.array_equal(got[b * rpb:(b + 1) * rpb], oracle.reduce_f32_ordered(W[b])), f"band {b}"
+
+
+def draw_codec_shapes(n, seed):
+    rng = np.random.RandomState(seed)
+    return [(int(rng.randint(1, 600)), 16 * int(rng.randint(1, 600)), float(10.0 ** rng.uniform(-20, 20)),
+             bool(rng.rand() < 0.5)) for _ in range(n)]
+
+
+CODEC_CASES = draw_codec_shapes(8, 7400)
+
+
+@pytest.mark.parametrize("M,N,sigma,bf16", CODEC_CASES,
+                         ids=[f"M{M}-N{N}-s{sigma:.0e}-{'bf16' if b else 'f32'}" for M, N, sigma, b in CODEC_CASES])
+def test_random_row_codec(g, ctx, M, N, sigma, bf16):
+    x = synthetic.normal(M + N, synthetic.TID_X, 3, (M, N), sigma=sigma)
+    if bf16:
+        xt = torch.from_numpy(x).to(torch.bfloat16)
+        x = xt.to(torch.float32).numpy()          # the codec sees exactly these values
+        xd = xt.cuda()
+    else:
+        xd = dev(x)
+    q = torch.empty((M, N), dtype=torch.uint8, device="cuda")
+    s = torch.empty((M,), dtype=torch.float32, device="cuda")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    g.rowquant_e4m3(ctx, xd, q, s)
+    g.rowdequant_e4m3(ctx, q, s, y)
+    torch.cuda.synchronize()
+    assert g.gemmar_status(ctx)[0] == 0
+    q_ref, s_ref = oracle.rowquant(x)
+    assert np.array_equal(s.cpu().numpy(), s_ref)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), oracle.rowdequant(q_ref, s_ref))

@@ -7,7 +7,8 @@ import pytest
 import torch
 
 import oracle
-from helpers import blockscale_operands, check_bf16_output, mx_operands, ptpc_operands, rel_l2
+from helpers import (blockscale_operands, check_bf16_output, check_f32_output, mx_operands,
+                     ptpc_operands, rel_l2)
 
 pytestmark = pytest.mark.gpu
 
@@ -38,17 +39,6 @@ def status_ok(g, ctx):
     torch.cuda.synchronize()
     code, detail = g.gemmar_status(ctx)
     assert code == 0, f"device status {code} at site {detail}"
-
-
-def check_f32_output(got, ref, what):
-    # fp32 accumulation and promotion against fp64: a few fp32 roundings of the
-    # magnitudes involved
-    got = np.asarray(got, np.float64)
-    scale = np.sqrt(np.mean(ref ** 2))
-    err = np.abs(got - ref)
-    assert np.all(np.isfinite(got)), what
-    assert rel_l2(got, ref) <= 2e-6, (what, rel_l2(got, ref))
-    assert np.all(err <= 1e-5 * np.abs(ref) + 2e-5 * scale), (what, err.max())
 
 
 # ------------------------------------------------------------ single-slice GEMMs
