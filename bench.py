@@ -12,7 +12,8 @@ ranks); `us_per_layer` is the same time per step.  Alongside: the GEMM
 kernel's roofline fraction (phase events inside the timed region), the band
 reduce's and the row codec's HBM fractions, the mxfp8 and M=8192 layers, an
 end-to-end number through the public API with host buffers, the oracle timed
-on this host's cores on a bounded sample, and the SM clocks seen meanwhile.
+on this host's cores on a bounded sample (and the GPU path checked against it
+on that sample: `validation`), and the SM clocks seen meanwhile.
 
 --impl reference times the oracle (the only reference this method has) on
 bounded samples of the same workload, on the host cores, rank 0 only.
@@ -164,25 +165,57 @@ def oracle_sample(rows_per_band, n_cols, seed=0):
     return A, sa, B, sb, rows, flops(P_HEAD, len(rows), n_cols, K_HEAD)
 
 
-def time_oracle(sample):
+def time_oracle(sample, want_ref=False):
     import oracle
     A, sa, B, sb, rows, fl = sample
     t0 = time.perf_counter()
-    oracle.gemm_reduce(A, sa, B, sb, 0, want_ref=False)
+    ref, _ = oracle.gemm_reduce(A, sa, B, sb, 0, want_ref=want_ref)
     dt = time.perf_counter() - t0
-    return dt, fl
+    return (dt, fl, ref) if want_ref else (dt, fl)
 
 
-def cpu_baseline_leg():
+def validate_on_sample(g, dev, sample, ref):
+    """The fused band path run on the oracle's sample (its rows as one layer of
+    P_HEAD bands), against the oracle's fp64 result."""
+    import numpy as np
+    import torch
+    A, sa, B, sb, _, _ = sample
+    Ms, Ns = A[0].shape[0], B[0].shape[0]
+    ctx = g.gemmar_create(dev.index, Ms, Ns, K_HEAD, P_HEAD, flags=g.GEMMAR_NO_SELF_TEST)
+    try:
+        up = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        out = torch.empty((Ms, Ns), dtype=torch.bfloat16, device=dev)
+        g.fused_gemm_reduce(ctx, [up(a) for a in A], [up(x) for x in sa], [up(b) for b in B], [up(x) for x in sb],
+                            out, bands=P_HEAD)
+        torch.cuda.synchronize(dev)
+        code, _ = g.gemmar_status(ctx)
+        got = out.float().cpu().numpy().astype(np.float64)
+    finally:
+        ctx.close()
+    err = np.abs(got - ref)
+    rel_l2 = float(np.linalg.norm(err) / np.linalg.norm(ref))
+    over = float(np.max(err / (1e-2 * np.abs(ref) + 1e-3)))
+    return {"rel_l2": rel_l2, "max_err_over_bound": over,
+            "validated": bool(code == 0 and rel_l2 <= 4e-3 and over <= 1.0),
+            "what": f"fused band path on the oracle's sample ({Ms} rows as {P_HEAD} bands x {Ns} columns, "
+                    f"P={P_HEAD}, K={K_HEAD}) against the fp64 oracle; bounds relL2 <= 4e-3 and "
+                    "|err| <= 1e-2|ref| + 1e-3 per element (max_err_over_bound <= 1)"}
+
+
+def cpu_baseline_leg(g=None, dev=None):
+    """The oracle timed on a bounded sample of the headline workload; with the
+    library and a device, also the GPU path checked on that sample."""
     import oracle
     rpb, ncols = 256, 7168           # 2048 rows x all columns: ~5e11 flop, 10-20 s on 16 cores
     sample = oracle_sample(rpb, ncols)
-    dt, fl = time_oracle(sample)
+    dt, fl, ref = time_oracle(sample, want_ref=True)
     tflops = fl / dt / 1e12
-    return {"value": tflops, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{rpb * P_HEAD} of {M_HEAD} rows ({rpb} per band) x {ncols} of {N_HEAD} output columns, "
-                      f"all {P_HEAD} slices, K={K_HEAD}: {fl:.3g} flop in {dt:.2f} s",
-            "us_per_layer_extrapolated": dt * flops(P_HEAD, M_HEAD, N_HEAD, K_HEAD) / fl * 1e6}
+    leg = {"value": tflops, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+           "sample": f"{rpb * P_HEAD} of {M_HEAD} rows ({rpb} per band) x {ncols} of {N_HEAD} output columns, "
+                     f"all {P_HEAD} slices, K={K_HEAD}: {fl:.3g} flop in {dt:.2f} s",
+           "us_per_layer_extrapolated": dt * flops(P_HEAD, M_HEAD, N_HEAD, K_HEAD) / fl * 1e6}
+    validation = validate_on_sample(g, dev, sample, ref) if g is not None else None
+    return leg, validation
 
 
 def run_reference(args, rank, world):
@@ -594,9 +627,9 @@ def run_ours(args, rank, world, local_rank):
     if code != 0:
         raise RuntimeError(f"device status {g.STATUS_NAMES.get(code)} at site {detail}")
 
-    cpu = None
+    cpu, validation = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_leg()
+        cpu, validation = cpu_baseline_leg(g, dev)
 
     if rank == 0:
         line = {
@@ -645,6 +678,7 @@ def run_ours(args, rank, world, local_rank):
             "gpu_launches": 2 * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "validation": validation,
         }
         print(json.dumps(line), flush=True)
     ctx.close()
