@@ -564,7 +564,7 @@ GEMMAR_API int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A
         } else {
             CUDA_OK(launch_band_reduce_blocked(ctx->W, out, P, M, N, bands, bn, ctx->band_done, expected,
                                                inkernel ? claim : nullptr, ctx->status, ctx->timeout_ns,
-                                               ctx->num_sms * 8, st));
+                                               ctx->num_sms, st));
         }
     }
     mark(ctx, GEMMAR_PHASE_QUANTIZE, st);

@@ -131,7 +131,7 @@ cudaError_t launch_band_reduce_quant(const float *W, const uint16_t *out, int P,
 cudaError_t launch_band_reduce_blocked(const float *W, uint16_t *out, int P, int64_t M, int64_t N, int bands,
                                        int bn, const uint32_t *band_done, uint32_t expected,
                                        const uint32_t *claimed, ptx::DevStatus *status,
-                                       uint64_t timeout_ns, int grid_blocks, cudaStream_t s);
+                                       uint64_t timeout_ns, int num_sms, cudaStream_t s);   // one wave of CTAs
 // Floats of blocked partials a fused call needs (ragged bands pad tiles to 128 rows).
 inline int64_t blocked_partial_floats(int P, int64_t M, int bands, int64_t N)
 {

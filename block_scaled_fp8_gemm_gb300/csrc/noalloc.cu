@@ -160,7 +160,7 @@ extern "C" __attribute__((visibility("default"))) int fused_gemm_reduce_noalloc(
         return GEMMAR_ERR_CUDA;
     const uint32_t expected = pl.band_signals;
     if (launch_band_reduce_blocked(s->partials, out, P, M, N, bands, bn, s->band_done, expected, claim, s->status,
-                                   kTimeoutNs, s->num_sms * 8, st) != cudaSuccess)
+                                   kTimeoutNs, s->num_sms, st) != cudaSuccess)
         return GEMMAR_ERR_CUDA;
     return GEMMAR_OK;
 }

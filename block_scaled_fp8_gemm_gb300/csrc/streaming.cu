@@ -4,6 +4,8 @@
 // kernels sized in multiples of the SM count.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "kernels.h"
 
 namespace gemmar {
@@ -705,19 +707,42 @@ cudaError_t launch_band_reduce(const float *W, uint16_t *out, int P, int64_t M, 
     return cudaGetLastError();
 }
 
+// CTAs of band_reduce_blocked_kernel<P> resident per SM, per device (0: not asked yet).
+std::atomic<int> g_blocked_per_sm[64][kMaxP + 1];
+
+template <int P>
+int blocked_per_sm()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 1;
+    int n = g_blocked_per_sm[dev][P].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, band_reduce_blocked_kernel<P>, 256, 0) != cudaSuccess ||
+            n < 1)
+            n = 1;
+        g_blocked_per_sm[dev][P].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 cudaError_t launch_band_reduce_blocked(const float *W, uint16_t *out, int P, int64_t M, int64_t N, int bands,
                                        int bn, const uint32_t *band_done, uint32_t expected,
                                        const uint32_t *claimed, DevStatus *status, uint64_t timeout_ns,
-                                       int grid_blocks, cudaStream_t s)
+                                       int num_sms, cudaStream_t s)
 {
     const int rpb = (int)(M / bands), mtpb = (rpb + 127) / 128, ntn = (int)(N / bn);
     const float4 *w4 = reinterpret_cast<const float4 *>(W);
-    dim3 grid(grid_blocks), block(256);
+    // one wave: every CTA resident from the start, none left for a partial second
+    // wave (its warps stride over the blocks, so the count only sets the schedule)
+    const dim3 block(256);
 #define GEMMAR_REDUCE_BLK_CASE(PP)                                                                                \
-    case PP:                                                                                                      \
+    case PP: {                                                                                                    \
+        const dim3 grid((unsigned)(num_sms * blocked_per_sm<PP>()));                                              \
         band_reduce_blocked_kernel<PP><<<grid, block, 0, s>>>(w4, out, (int)M, (int)N, bands, rpb, mtpb, ntn, bn, \
                                                               band_done, expected, claimed, status, timeout_ns);   \
-        break;
+        break;                                                                                                    \
+    }
     switch (P) {
         GEMMAR_REDUCE_BLK_CASE(1) GEMMAR_REDUCE_BLK_CASE(2) GEMMAR_REDUCE_BLK_CASE(3) GEMMAR_REDUCE_BLK_CASE(4)
         GEMMAR_REDUCE_BLK_CASE(5) GEMMAR_REDUCE_BLK_CASE(6) GEMMAR_REDUCE_BLK_CASE(7) GEMMAR_REDUCE_BLK_CASE(8)
