@@ -707,23 +707,29 @@ cudaError_t launch_band_reduce(const float *W, uint16_t *out, int P, int64_t M, 
     return cudaGetLastError();
 }
 
-// CTAs of band_reduce_blocked_kernel<P> resident per SM, per device (0: not asked yet).
-std::atomic<int> g_blocked_per_sm[64][kMaxP + 1];
-
-template <int P>
-int blocked_per_sm()
+// CTAs of `kernel` (256 threads, no dynamic shared memory) resident per SM on the
+// current device, asked once per device and kept in `cache` (0: not asked yet).
+template <typename Kernel>
+int resident_per_sm(Kernel kernel, std::atomic<int> (&cache)[64])
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return 1;
-    int n = g_blocked_per_sm[dev][P].load(std::memory_order_relaxed);
+    int n = cache[dev].load(std::memory_order_relaxed);
     if (n == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, band_reduce_blocked_kernel<P>, 256, 0) != cudaSuccess ||
-            n < 1)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, 256, 0) != cudaSuccess || n < 1)
             n = 1;
-        g_blocked_per_sm[dev][P].store(n, std::memory_order_relaxed);
+        cache[dev].store(n, std::memory_order_relaxed);
     }
     return n;
+}
+
+std::atomic<int> g_blocked_per_sm[kMaxP + 1][64];
+
+template <int P>
+int blocked_per_sm()
+{
+    return resident_per_sm(band_reduce_blocked_kernel<P>, g_blocked_per_sm[P]);
 }
 
 cudaError_t launch_band_reduce_blocked(const float *W, uint16_t *out, int P, int64_t M, int64_t N, int bands,
