@@ -1,7 +1,8 @@
 """CPU oracle for the block-scaled fp8 wo_b path (plain C in ``oracle.c``, fp64).
 
-TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
-CPU-baseline leg of ``bench.py`` are the only callers.  The CUDA library never
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()``, and
+``bench.py``'s CPU-baseline leg (which also checks the GPU result on its sample)
+and its ``--impl reference`` arm are the only callers.  The CUDA library never
 imports, links or executes anything here, and this module imports nothing
 from the CUDA package.
 
