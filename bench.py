@@ -446,6 +446,20 @@ def run_ours(args, rank, world, local_rank):
         "note": "GEMMAR_SERIAL_REDUCE: the GEMM reduces nothing while it runs; band_reduce sums every "
                 "block after it (same output bits)"}
 
+    # ---- the band_reduce entry point on its own: row-major fp32 partials
+    # [bands][P][M/bands][N] of the headline size, summed to bf16
+    W_rm = torch.randn((P, M, N), dtype=torch.float32, device=dev)
+    out_br = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    step_br = lambda: g.band_reduce(ctx, W_rm, P, M, N, P, out_br)
+    for _ in range(2):
+        step_br()
+    ms_br = time_steps(step_br, max(5, args.steps // 10), stream)
+    del W_rm, out_br
+    extra["band_reduce_entry"] = {
+        "us": ms_br * 1e3, "GB/s": reduce_bytes / (ms_br * 1e-3) / 1e9,
+        "frac_of_measured_hbm": reduce_bytes / (ms_br * 1e-3) / 1e9 / peaks["hbm_gbs"],
+        "what": "band_reduce called alone on row-major fp32 partials [8 bands][8 slices][2048][7168] (3.76 GB)"}
+
     # ---- the fp8 wire layer (config 3) and the row codec alone
     step_wire = lambda: g.fused_gemm_reduce(ctx, A, sa, B, sb, out, bands=P, flags=g.GEMMAR_FP8_WIRE)
     for _ in range(2):

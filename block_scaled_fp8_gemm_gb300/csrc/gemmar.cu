@@ -404,7 +404,7 @@ GEMMAR_API int band_reduce(gemmar_ctx *ctx, const float *W, int P, int64_t M, in
         return GEMMAR_ERR_SHAPE;
     if (!aligned16(W) || !aligned16(out))
         return GEMMAR_ERR_ALIGN;
-    CUDA_OK(launch_band_reduce(W, out, P, M, N, bands, nullptr, 0, ctx->status, ctx->timeout_ns, ctx->num_sms * 8,
+    CUDA_OK(launch_band_reduce(W, out, P, M, N, bands, nullptr, 0, ctx->status, ctx->timeout_ns, ctx->num_sms,
                                as_stream(stream)));
     return GEMMAR_OK;
 }

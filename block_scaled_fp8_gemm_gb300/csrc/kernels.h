@@ -116,7 +116,7 @@ cudaError_t launch_mx_repack(const uint8_t *const *ea, const uint8_t *const *eb,
 // Streaming kernels.
 cudaError_t launch_band_reduce(const float *W, uint16_t *out, int P, int64_t M, int64_t N, int bands,
                                const uint32_t *band_done, uint32_t expected, ptx::DevStatus *status,
-                               uint64_t timeout_ns, int grid_blocks, cudaStream_t s);
+                               uint64_t timeout_ns, int num_sms, cudaStream_t s);
 // The same reduce over the fused path's tile-blocked partials (layout: epilogue.cuh).
 // claimed (device, [bands], may be nullptr): in band b the blocks below claimed[b]
 // were already reduced by the GEMM kernel's reducer warps (GemmOut::reduce_next).

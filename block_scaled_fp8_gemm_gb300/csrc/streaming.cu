@@ -687,26 +687,6 @@ __global__ void mx_repack_b_kernel(SlicePtrs eb, int P, int N, int K, int BN, ui
 
 // ------------------------------------------------------------------ launchers
 
-cudaError_t launch_band_reduce(const float *W, uint16_t *out, int P, int64_t M, int64_t N, int bands,
-                               const uint32_t *band_done, uint32_t expected, DevStatus *status,
-                               uint64_t timeout_ns, int grid_blocks, cudaStream_t s)
-{
-    const int64_t rpb = M / bands;
-    dim3 grid(grid_blocks), block(256);
-#define GEMMAR_REDUCE_CASE(PP)                                                                            \
-    case PP:                                                                                              \
-        band_reduce_kernel<PP><<<grid, block, 0, s>>>(W, out, rpb, N, bands, band_done, expected, status, \
-                                                      timeout_ns);                                        \
-        break;
-    switch (P) {
-        GEMMAR_REDUCE_CASE(1) GEMMAR_REDUCE_CASE(2) GEMMAR_REDUCE_CASE(3) GEMMAR_REDUCE_CASE(4)
-        GEMMAR_REDUCE_CASE(5) GEMMAR_REDUCE_CASE(6) GEMMAR_REDUCE_CASE(7) GEMMAR_REDUCE_CASE(8)
-        default: return cudaErrorInvalidValue;
-    }
-#undef GEMMAR_REDUCE_CASE
-    return cudaGetLastError();
-}
-
 // CTAs of `kernel` (256 threads, no dynamic shared memory) resident per SM on the
 // current device, asked once per device and kept in `cache` (0: not asked yet).
 template <typename Kernel>
@@ -724,7 +704,32 @@ int resident_per_sm(Kernel kernel, std::atomic<int> (&cache)[64])
     return n;
 }
 
+std::atomic<int> g_plain_per_sm[kMaxP + 1][64];
 std::atomic<int> g_blocked_per_sm[kMaxP + 1][64];
+
+cudaError_t launch_band_reduce(const float *W, uint16_t *out, int P, int64_t M, int64_t N, int bands,
+                               const uint32_t *band_done, uint32_t expected, DevStatus *status,
+                               uint64_t timeout_ns, int num_sms, cudaStream_t s)
+{
+    const int64_t rpb = M / bands;
+    // two whole waves of resident CTAs (measured at the headline size: 576 us
+    // against 581 for one wave and 591 for 8 CTAs per SM, 2.67 waves)
+    const dim3 block(256);
+#define GEMMAR_REDUCE_CASE(PP)                                                                            \
+    case PP: {                                                                                            \
+        const dim3 grid((unsigned)(2 * num_sms * resident_per_sm(band_reduce_kernel<PP>, g_plain_per_sm[PP]))); \
+        band_reduce_kernel<PP><<<grid, block, 0, s>>>(W, out, rpb, N, bands, band_done, expected, status, \
+                                                      timeout_ns);                                        \
+        break;                                                                                            \
+    }
+    switch (P) {
+        GEMMAR_REDUCE_CASE(1) GEMMAR_REDUCE_CASE(2) GEMMAR_REDUCE_CASE(3) GEMMAR_REDUCE_CASE(4)
+        GEMMAR_REDUCE_CASE(5) GEMMAR_REDUCE_CASE(6) GEMMAR_REDUCE_CASE(7) GEMMAR_REDUCE_CASE(8)
+        default: return cudaErrorInvalidValue;
+    }
+#undef GEMMAR_REDUCE_CASE
+    return cudaGetLastError();
+}
 
 template <int P>
 int blocked_per_sm()
