@@ -107,7 +107,6 @@ __global__ void __launch_bounds__(256) band_reduce_blocked_kernel(const float4 *
                                                                   uint32_t expected, const uint32_t *claimed,
                                                                   DevStatus *status, uint64_t timeout_ns)
 {
-    __shared__ int band_ok;
     __shared__ __align__(16) uint32_t stage[8][32 * 16];   // per warp: 32 rows x 64 bytes
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nchunk = bn / 32;
@@ -118,24 +117,24 @@ __global__ void __launch_bounds__(256) band_reduce_blocked_kernel(const float4 *
     uint32_t *st = stage[warp];
     for (int b = 0; b < bands; ++b) {
         if (band_done != nullptr) {
-            if (threadIdx.x == 0) {
-                int ok = 1;
-                if (ld_acquire(band_done + b) < expected) {
-                    const uint64_t t0 = globaltimer();
-                    while (ld_acquire(band_done + b) < expected) {
-                        if (*(volatile int *)&status->code != 0) { ok = 0; break; }
-                        if (globaltimer() - t0 > timeout_ns) {
-                            report(status, kErrTimeout, SITE_REDUCE_BAND);
-                            ok = 0;
-                            break;
-                        }
-                        __nanosleep(256);
+            // each warp checks the band itself: no CTA-wide barrier per band, so a
+            // warp with fewer blocks in the last band moves on to the next one
+            int ok = 1;
+            if (lane == 0 && ld_acquire(band_done + b) < expected) {
+                const uint64_t t0 = globaltimer();
+                while (ld_acquire(band_done + b) < expected) {
+                    if (*(volatile int *)&status->code != 0) { ok = 0; break; }
+                    if (globaltimer() - t0 > timeout_ns) {
+                        report(status, kErrTimeout, SITE_REDUCE_BAND);
+                        ok = 0;
+                        break;
                     }
+                    __nanosleep(256);
                 }
-                band_ok = ok;
             }
-            __syncthreads();
-            if (!band_ok)
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            __syncwarp();
+            if (!ok)
                 return;
         }
         const int64_t blk0 = claimed != nullptr ? min64((int64_t)claimed[b], blocks_per_band) : 0;
