@@ -18,7 +18,7 @@
  *              benchmark", "Where the time goes", "The fp8 wire",
  *              "What fp8 costs, numerically".
  *
- * Readings taken where the pages are silent (each also listed in the design doc):
+ * Readings taken where the pages are silent:
  *   R1  "e4m3" is OCP E4M3FN: bias 7, no infinities, S.1111.111 is NaN,
  *       largest finite 448 -- the only e4m3 variant whose maximum is the 448
  *       of the pages' "amax/448" scale rule.

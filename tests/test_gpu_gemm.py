@@ -7,8 +7,8 @@ import pytest
 import torch
 
 import oracle
-from helpers import (blockscale_operands, check_bf16_output, check_f32_output, mx_operands,
-                     ptpc_operands, rel_l2)
+from helpers import (PAGES_BF16_WIRE_REL_L2, blockscale_operands, check_bf16_output,
+                     check_f32_output, mx_operands, ptpc_operands, rel_l2)
 
 pytestmark = pytest.mark.gpu
 
@@ -110,7 +110,7 @@ def test_fused_blockscale_vs_oracle(g, ctx, P, M, N, K, bands):
     ref, _ = oracle.gemm_reduce(A, sa, B, sb, 0)
     out = run_fused(g, ctx, A, sa, B, sb, g.GEMMAR_SCALE_BLOCK128, bands, flags=g.GEMMAR_DEBUG_CANARY)
     rl = check_bf16_output(out.float().cpu().numpy(), ref, f"fused P={P} M={M} N={N} K={K} bands={bands}")
-    assert rl < 2.35e-3      # fp32 partials stay below the pages' bf16-partial level
+    assert rl < PAGES_BF16_WIRE_REL_L2      # fp32 partials stay below the pages' bf16-partial level
 
 
 @pytest.mark.parametrize("P,M,N,K,bands", [(2, 256, 448, 256, 2), (4, 384, 256, 128, 4), (3, 600, 384, 256, 3)])
@@ -334,7 +334,7 @@ def test_fused_ptpc_band_onchip_bitwise(g, ctx, P, M, N, K, bands):
     ref, _ = oracle.gemm_reduce(A, sa, B, sb, 2)
     band = run_fused(g, ctx, A, sa, B, sb, g.GEMMAR_SCALE_PTPC, bands, flags=g.GEMMAR_DEBUG_CANARY)
     rl = check_bf16_output(band.float().cpu().numpy(), ref, f"ptpc band P={P} M={M} N={N} K={K}")
-    assert rl < 2.35e-3
+    assert rl < PAGES_BF16_WIRE_REL_L2
     onchip = run_fused(g, ctx, A, sa, B, sb, g.GEMMAR_SCALE_PTPC, bands,
                        flags=g.GEMMAR_FUSE_ONCHIP | g.GEMMAR_DEBUG_CANARY)
     assert torch.equal(onchip.view(torch.int16), band.view(torch.int16))
