@@ -81,10 +81,11 @@ _SIGS = {
     "band_reduce": (_I, [_P, _P, _I, _I64, _I64, _I, _P, _P]),
     "rowquant_e4m3": (_I, [_P, _P, _I, _I64, _I64, _P, _P, _P]),
     "rowdequant_e4m3": (_I, [_P, _P, _P, _I64, _I64, _P, _P]),
-    "quant_blockscale_e4m3": (_I, [_P, _P, _I64, _I64, _I, _P, _P, _P]),
-    "quant_mx_e4m3": (_I, [_P, _P, _I64, _I64, _P, _P, _P]),
+    "quant_blockscale_e4m3": (_I, [_P, _P, _I, _I64, _I64, _I, _P, _P, _P]),
+    "quant_mx_e4m3": (_I, [_P, _P, _I, _I64, _I64, _P, _P, _P]),
     "fused_gemm_reduce": (_I, [_P, _I, _PP, _PP, _PP, _PP, _I, _I64, _I64, _I64, _I, _U32, _P, _P]),
     "fused_gemm_reduce_noalloc": (_I, [_I, _PP, _PP, _PP, _PP, _I64, _I64, _I64, _I, _P, _P]),
+    "fused_gemm_reduce_noalloc_status": (_I, [ctypes.POINTER(_I)]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -264,16 +265,18 @@ def band_reduce(ctx: Context, W, P: int, M: int, N: int, bands: int, out, stream
            "band_reduce")
 
 
+def _xdtype(x) -> int:
+    if x.dtype == torch.bfloat16:
+        return GEMMAR_DTYPE_BF16
+    if x.dtype == torch.float32:
+        return GEMMAR_DTYPE_F32
+    raise TypeError(f"x must be bfloat16 or float32, got {x.dtype}")
+
+
 def rowquant_e4m3(ctx: Context, x, q, row_scale, stream=None) -> None:
     M, N = x.shape
-    if x.dtype == torch.bfloat16:
-        xd = GEMMAR_DTYPE_BF16
-    elif x.dtype == torch.float32:
-        xd = GEMMAR_DTYPE_F32
-    else:
-        raise TypeError(f"x must be bfloat16 or float32, got {x.dtype}")
-    _check(_lib.rowquant_e4m3(ctx.handle, _ptr(x, "x"), xd, M, N, _u8(q, "q"), _f32(row_scale, "row_scale"),
-                              _stream(stream)),
+    _check(_lib.rowquant_e4m3(ctx.handle, _ptr(x, "x"), _xdtype(x), M, N, _u8(q, "q"),
+                              _f32(row_scale, "row_scale"), _stream(stream)),
            "rowquant_e4m3")
 
 
@@ -285,15 +288,18 @@ def rowdequant_e4m3(ctx: Context, q, row_scale, y, stream=None) -> None:
 
 
 def quant_blockscale_e4m3(ctx: Context, x, group_rows: int, q, scales, stream=None) -> None:
+    """Blockscale quantiser of a bf16 or fp32 [R, C] matrix (group_rows 1 or 128)."""
     R, C = x.shape
-    _check(_lib.quant_blockscale_e4m3(ctx.handle, _f32(x, "x"), R, C, group_rows, _u8(q, "q"),
+    _check(_lib.quant_blockscale_e4m3(ctx.handle, _ptr(x, "x"), _xdtype(x), R, C, group_rows, _u8(q, "q"),
                                       _f32(scales, "scales"), _stream(stream)),
            "quant_blockscale_e4m3")
 
 
 def quant_mx_e4m3(ctx: Context, x, q, e8m0, stream=None) -> None:
+    """mxfp8 quantiser (ue8m0 per 1x32) of a bf16 or fp32 [R, C] matrix."""
     R, C = x.shape
-    _check(_lib.quant_mx_e4m3(ctx.handle, _f32(x, "x"), R, C, _u8(q, "q"), _u8(e8m0, "e8m0"), _stream(stream)),
+    _check(_lib.quant_mx_e4m3(ctx.handle, _ptr(x, "x"), _xdtype(x), R, C, _u8(q, "q"), _u8(e8m0, "e8m0"),
+                              _stream(stream)),
            "quant_mx_e4m3")
 
 
@@ -333,3 +339,11 @@ def fused_gemm_reduce_noalloc(A: Sequence, sa: Sequence, B: Sequence, sb: Sequen
                                           arr([_u8(b, "B[p]") for b in B]), arr([_f32(s, "sb[p]") for s in sb]),
                                           M, N, K, bands, _bf16(out, "out"), _stream(stream)),
            "fused_gemm_reduce_noalloc")
+
+
+def fused_gemm_reduce_noalloc_status():
+    """(code, detail) of the last fused_gemm_reduce_noalloc call on the current
+    device; call after its work has completed (code 0: every wait finished)."""
+    d = ctypes.c_int(0)
+    code = int(_lib.fused_gemm_reduce_noalloc_status(ctypes.byref(d)))
+    return code, int(d.value)

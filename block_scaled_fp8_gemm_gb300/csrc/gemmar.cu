@@ -441,35 +441,37 @@ GEMMAR_API int rowdequant_e4m3(gemmar_ctx *ctx, const uint8_t *q, const float *r
     return GEMMAR_OK;
 }
 
-GEMMAR_API int quant_blockscale_e4m3(gemmar_ctx *ctx, const float *x, int64_t R, int64_t C, int group_rows,
-                                     uint8_t *q, float *scales, void *stream)
+GEMMAR_API int quant_blockscale_e4m3(gemmar_ctx *ctx, const void *x, int x_dtype, int64_t R, int64_t C,
+                                     int group_rows, uint8_t *q, float *scales, void *stream)
 {
     int rc = check_ctx(ctx);
     if (rc)
         return rc;
-    if (!x || !q || !scales || R < 1 || C < 1 || (group_rows != 1 && group_rows != 128))
+    if (!x || !q || !scales || R < 1 || C < 1 || (group_rows != 1 && group_rows != 128) ||
+        (x_dtype != GEMMAR_DTYPE_F32 && x_dtype != GEMMAR_DTYPE_BF16))
         return GEMMAR_ERR_ARG;
     if (C % 128 != 0)
         return GEMMAR_ERR_SHAPE;
     if (!aligned16(x) || !aligned16(q) || !aligned16(scales))
         return GEMMAR_ERR_ALIGN;
-    CUDA_OK(launch_quant_blockscale(x, R, C, group_rows, q, scales, ctx->num_sms, as_stream(stream)));
+    CUDA_OK(launch_quant_blockscale(x, x_dtype == GEMMAR_DTYPE_BF16, R, C, group_rows, q, scales, ctx->num_sms,
+                                    as_stream(stream)));
     return GEMMAR_OK;
 }
 
-GEMMAR_API int quant_mx_e4m3(gemmar_ctx *ctx, const float *x, int64_t R, int64_t C, uint8_t *q, uint8_t *e8m0,
-                             void *stream)
+GEMMAR_API int quant_mx_e4m3(gemmar_ctx *ctx, const void *x, int x_dtype, int64_t R, int64_t C, uint8_t *q,
+                             uint8_t *e8m0, void *stream)
 {
     int rc = check_ctx(ctx);
     if (rc)
         return rc;
-    if (!x || !q || !e8m0 || R < 1 || C < 1)
+    if (!x || !q || !e8m0 || R < 1 || C < 1 || (x_dtype != GEMMAR_DTYPE_F32 && x_dtype != GEMMAR_DTYPE_BF16))
         return GEMMAR_ERR_ARG;
     if (C % 32 != 0)
         return GEMMAR_ERR_SHAPE;
     if (!aligned16(x) || !aligned16(q) || !aligned16(e8m0))
         return GEMMAR_ERR_ALIGN;
-    CUDA_OK(launch_quant_mx(x, R, C, q, e8m0, ctx->num_sms, as_stream(stream)));
+    CUDA_OK(launch_quant_mx(x, x_dtype == GEMMAR_DTYPE_BF16, R, C, q, e8m0, ctx->num_sms, as_stream(stream)));
     return GEMMAR_OK;
 }
 

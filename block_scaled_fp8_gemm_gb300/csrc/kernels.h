@@ -142,9 +142,10 @@ cudaError_t launch_rowquant(const void *x, int x_is_bf16, int64_t M, int64_t N, 
                             int num_sms, cudaStream_t st);
 cudaError_t launch_rowdequant(const uint8_t *q, const float *s, int64_t M, int64_t N, uint16_t *y, int num_sms,
                               cudaStream_t st);
-cudaError_t launch_quant_blockscale(const float *x, int64_t R, int64_t C, int group_rows, uint8_t *q,
+// Device quantisers; x is fp32 or (x_is_bf16) bf16.
+cudaError_t launch_quant_blockscale(const void *x, int x_is_bf16, int64_t R, int64_t C, int group_rows, uint8_t *q,
                                     float *scales, int num_sms, cudaStream_t st);
-cudaError_t launch_quant_mx(const float *x, int64_t R, int64_t C, uint8_t *q, uint8_t *e8, int num_sms,
+cudaError_t launch_quant_mx(const void *x, int x_is_bf16, int64_t R, int64_t C, uint8_t *q, uint8_t *e8, int num_sms,
                             cudaStream_t st);
 
 }  // namespace gemmar

@@ -164,3 +164,25 @@ extern "C" __attribute__((visibility("default"))) int fused_gemm_reduce_noalloc(
         return GEMMAR_ERR_CUDA;
     return GEMMAR_OK;
 }
+
+extern "C" __attribute__((visibility("default"))) int fused_gemm_reduce_noalloc_status(int *detail)
+{
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess)
+        return GEMMAR_ERR_CUDA;
+    if (device < 0 || device >= kMaxDevices)
+        return GEMMAR_ERR_DEVICE;
+    ptx::DevStatus *dst = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_scratch_mutex);
+        if (!g_scratch[device].ready)
+            return GEMMAR_ERR_DEVICE;   // no call on this device yet
+        dst = g_scratch[device].status;
+    }
+    ptx::DevStatus st{};
+    if (cudaMemcpy(&st, dst, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMMAR_ERR_CUDA;
+    if (detail)
+        *detail = st.detail;
+    return st.code == 0 ? GEMMAR_OK : st.code;
+}

@@ -507,52 +507,121 @@ __global__ void __launch_bounds__(256) rowdequant_kernel(const uint8_t *__restri
 }
 
 // --------------------------------------------------------------------------
-// Blockscale quantisers.  1x128: one warp per (row, 128-group), 4 values per
-// lane.  128x128: one 256-thread CTA per block.  s = fp32(amax/448),
-// codes = e4m3_rn_sat(fp32(x/s)); zero group -> s = 0, +0 codes.
+// Blockscale quantisers, on fp32 or bf16 input (the call site quantises the
+// layer's bf16 activations itself).  Every lane loads 16 bytes: V = 4 fp32 or
+// 8 bf16 values (bf16 -> fp32 is exact, so both inputs meet the same fp32
+// arithmetic).  s = fp32(amax/448), codes = e4m3_rn_sat(fp32(x/s)); a zero
+// group gives s = 0 and +0 codes.
 // --------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) quant_1x128_kernel(const float *__restrict__ x, int64_t R, int64_t C,
+template <bool BF16>
+struct Lane16 {
+    static constexpr int V = BF16 ? 8 : 4;   // values per 16-byte lane load
+    float v[V];
+    __device__ __forceinline__ void load(const void *x, int64_t e)
+    {
+        if constexpr (BF16) {
+            const uint4 w = __ldcs(reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(x) + e));
+            v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+            v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z); v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+        } else {
+            const float4 a = __ldcs(reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) + e));
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        }
+    }
+    __device__ __forceinline__ float amax() const
+    {
+        float m = fabsf(v[0]);
+#pragma unroll
+        for (int i = 1; i < V; ++i)
+            m = fmaxf(m, fabsf(v[i]));
+        return m;
+    }
+    // the V codes of this lane, stored with one 4- or 8-byte write
+    __device__ __forceinline__ void store_codes(uint8_t *q, int64_t e, const Enc &enc) const
+    {
+        const uint32_t lo = enc(v[0], v[1], v[2], v[3]);
+        if constexpr (BF16)
+            *reinterpret_cast<uint2 *>(q + e) = make_uint2(lo, enc(v[4], v[5], v[6], v[7]));
+        else
+            *reinterpret_cast<uint32_t *>(q + e) = lo;
+    }
+};
+
+// max over the L lanes of an aligned L-lane segment of the warp; only the
+// lanes of that segment need to take part
+template <int L>
+__device__ __forceinline__ float segment_max(float m)
+{
+    uint32_t mask = 0xFFFFFFFFu;
+    if constexpr (L < 32)
+        mask = ((1u << L) - 1u) << ((threadIdx.x & 31) & ~(L - 1));
+#pragma unroll
+    for (int o = L / 2; o > 0; o >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(mask, m, o));
+    return m;
+}
+
+// 1x128: an aligned segment of 128/V lanes per (row, 128-group); a warp covers
+// 32V/128 groups per step and takes two steps at once (loads in flight).
+template <bool BF16>
+__global__ void __launch_bounds__(256) quant_1x128_kernel(const void *__restrict__ x, int64_t R, int64_t C,
                                                           uint8_t *__restrict__ q, float *__restrict__ scales)
 {
+    using L16 = Lane16<BF16>;
+    constexpr int L = 128 / L16::V;   // lanes per group
+    constexpr int GPW = 32 / L;       // groups per warp step
     const int lane = threadIdx.x & 31;
     const int64_t G = C / 128;
     const int64_t ngroups = R * G;
     const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t gi = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); gi < ngroups; gi += warps_total) {
-        const int64_t r = gi / G, g = gi % G;
-        const int64_t e = r * C + g * 128 + lane * 4;
-        const float4 v = *reinterpret_cast<const float4 *>(x + e);
-        float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    const int64_t w0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    for (int64_t step = w0 * 2; step * GPW < ngroups; step += warps_total * 2) {
+        int64_t gi[2], e[2];
+        L16 d[2];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-        const float sc = __fdiv_rn(amax, 448.0f);
-        if (lane == 0)
-            scales[gi] = sc;
-        *reinterpret_cast<uint32_t *>(q + e) = Enc(sc)(v.x, v.y, v.z, v.w);
+        for (int u = 0; u < 2; ++u) {
+            gi[u] = (step + u) * GPW + lane / L;
+            e[u] = (gi[u] / G) * C + (gi[u] % G) * 128 + (lane % L) * L16::V;
+            if (gi[u] < ngroups)
+                d[u].load(x, e[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const float m = segment_max<L>(gi[u] < ngroups ? d[u].amax() : 0.0f);
+            if (gi[u] < ngroups) {
+                const float sc = __fdiv_rn(m, 448.0f);
+                if (lane % L == 0)
+                    scales[gi[u]] = sc;
+                d[u].store_codes(q, e[u], Enc(sc));
+            }
+        }
     }
 }
 
-__global__ void __launch_bounds__(256) quant_128x128_kernel(const float *__restrict__ x, int64_t R, int64_t C,
+// 128x128: one 256-thread CTA per block; each warp row-step covers 32V/128 rows.
+template <bool BF16>
+__global__ void __launch_bounds__(256) quant_128x128_kernel(const void *__restrict__ x, int64_t R, int64_t C,
                                                             uint8_t *__restrict__ q, float *__restrict__ scales)
 {
+    using L16 = Lane16<BF16>;
+    constexpr int L = 128 / L16::V;   // lanes per row of the block
+    constexpr int RPW = 32 / L;       // rows per warp step
     __shared__ float red[8];
     const int64_t G = C / 128;
     const int64_t nblk = ((R + 127) / 128) * G;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int sub = lane / L, col = (lane % L) * L16::V;
     for (int64_t bi = blockIdx.x; bi < nblk; bi += gridDim.x) {
         const int64_t br = bi / G, bc = bi % G;
         const int64_t r0 = br * 128;
         const int rows = (int)min64(128, R - r0);
-        // thread covers column quad (tid & 31)*4 of rows (tid >> 5) + 8*j
         float amax = 0.0f;
-        for (int rr = warp; rr < rows; rr += 8) {
-            const float4 v = *reinterpret_cast<const float4 *>(x + (r0 + rr) * C + bc * 128 + lane * 4);
-            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        for (int rr = warp * RPW + sub; rr < rows; rr += 8 * RPW) {
+            L16 d;
+            d.load(x, (r0 + rr) * C + bc * 128 + col);
+            amax = fmaxf(amax, d.amax());
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        amax = segment_max<32>(amax);
         if (lane == 0)
             red[warp] = amax;
         __syncthreads();
@@ -564,10 +633,11 @@ __global__ void __launch_bounds__(256) quant_128x128_kernel(const float *__restr
         if (tid == 0)
             scales[bi] = sc;
         const Enc enc(sc);
-        for (int rr = warp; rr < rows; rr += 8) {
-            const int64_t e = (r0 + rr) * C + bc * 128 + lane * 4;
-            const float4 v = *reinterpret_cast<const float4 *>(x + e);
-            *reinterpret_cast<uint32_t *>(q + e) = enc(v.x, v.y, v.z, v.w);
+        for (int rr = warp * RPW + sub; rr < rows; rr += 8 * RPW) {
+            const int64_t e = (r0 + rr) * C + bc * 128 + col;
+            L16 d;
+            d.load(x, e);
+            d.store_codes(q, e, enc);
         }
         __syncthreads();
     }
@@ -599,31 +669,37 @@ __device__ __forceinline__ float inv_scale_of(uint32_t byte)
     return byte == 254u ? __uint_as_float(0x00400000u) : __uint_as_float((254u - byte) << 23);
 }
 
-// mx quantiser: 8 lanes per 32-wide group, 4 values per lane.
-__global__ void __launch_bounds__(256) quant_mx_kernel(const float *__restrict__ x, int64_t R, int64_t C,
+// mx quantiser: an aligned segment of 32/V lanes per 32-wide group (V values
+// per lane: 4 fp32 or 8 bf16).
+template <bool BF16>
+__global__ void __launch_bounds__(256) quant_mx_kernel(const void *__restrict__ x, int64_t R, int64_t C,
                                                        uint8_t *__restrict__ q, uint8_t *__restrict__ e8)
 {
-    const int64_t nquads = R * C / 4;
+    using L16 = Lane16<BF16>;
+    constexpr int L = 32 / L16::V;   // lanes per group
+    const int64_t nvec = R * C / L16::V;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    // the grid stride is a multiple of 32 threads, so the 8 lanes of one group stay together
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nquads; i += stride) {
-        const int64_t e = i * 4;
-        const float4 v = *reinterpret_cast<const float4 *>(x + e);
-        float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-        const uint32_t gmask = 0xFFu << (threadIdx.x & 24);
-        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 4));
+    // the grid stride is a multiple of 32 threads, so the lanes of one group stay together
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
+        const int64_t e = i * L16::V;
+        L16 d;
+        d.load(x, e);
+        const float amax = segment_max<L>(d.amax());
         const uint32_t b = ue8m0_of(__fdiv_rn(amax, 448.0f));
-        if ((threadIdx.x & 7) == 0)
+        if ((threadIdx.x & (L - 1)) == 0)
             e8[e / 32] = (uint8_t)b;
-        uint32_t w = 0;
+        uint32_t w[2] = {0u, 0u};
         if (amax != 0.0f) {
             const float inv = inv_scale_of(b);
-            w = e4m3x2_from_f32(__fmul_rn(v.x, inv), __fmul_rn(v.y, inv)) |
-                (e4m3x2_from_f32(__fmul_rn(v.z, inv), __fmul_rn(v.w, inv)) << 16);
+#pragma unroll
+            for (int h = 0; h < L16::V / 4; ++h)
+                w[h] = e4m3x2_from_f32(__fmul_rn(d.v[4 * h], inv), __fmul_rn(d.v[4 * h + 1], inv)) |
+                       (e4m3x2_from_f32(__fmul_rn(d.v[4 * h + 2], inv), __fmul_rn(d.v[4 * h + 3], inv)) << 16);
         }
-        *reinterpret_cast<uint32_t *>(q + e) = w;
+        if constexpr (BF16)
+            *reinterpret_cast<uint2 *>(q + e) = make_uint2(w[0], w[1]);
+        else
+            *reinterpret_cast<uint32_t *>(q + e) = w[0];
     }
 }
 
@@ -815,27 +891,37 @@ cudaError_t launch_rowdequant(const uint8_t *q, const float *s, int64_t M, int64
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_blockscale(const float *x, int64_t R, int64_t C, int group_rows, uint8_t *q,
+cudaError_t launch_quant_blockscale(const void *x, int x_is_bf16, int64_t R, int64_t C, int group_rows, uint8_t *q,
                                     float *scales, int num_sms, cudaStream_t st)
 {
     if (group_rows == 1) {
-        const int64_t need = (R * (C / 128) + 7) / 8;
+        const int64_t gpw = x_is_bf16 ? 2 : 1;   // groups per warp step; two steps per pass
+        const int64_t need = (R * (C / 128) + 16 * gpw - 1) / (16 * gpw);
         const int grid = (int)max64(1, min64(need, (int64_t)num_sms * 8));
-        quant_1x128_kernel<<<grid, 256, 0, st>>>(x, R, C, q, scales);
+        if (x_is_bf16)
+            quant_1x128_kernel<true><<<grid, 256, 0, st>>>(x, R, C, q, scales);
+        else
+            quant_1x128_kernel<false><<<grid, 256, 0, st>>>(x, R, C, q, scales);
     } else {
         const int64_t nblk = ((R + 127) / 128) * (C / 128);
         const int grid = (int)max64(1, min64(nblk, (int64_t)num_sms * 8));
-        quant_128x128_kernel<<<grid, 256, 0, st>>>(x, R, C, q, scales);
+        if (x_is_bf16)
+            quant_128x128_kernel<true><<<grid, 256, 0, st>>>(x, R, C, q, scales);
+        else
+            quant_128x128_kernel<false><<<grid, 256, 0, st>>>(x, R, C, q, scales);
     }
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_mx(const float *x, int64_t R, int64_t C, uint8_t *q, uint8_t *e8, int num_sms,
+cudaError_t launch_quant_mx(const void *x, int x_is_bf16, int64_t R, int64_t C, uint8_t *q, uint8_t *e8, int num_sms,
                             cudaStream_t st)
 {
-    const int64_t need = (R * C / 4 + 255) / 256;
+    const int64_t need = (R * C / (x_is_bf16 ? 8 : 4) + 255) / 256;
     const int grid = (int)max64(1, min64(need, (int64_t)num_sms * 8));
-    quant_mx_kernel<<<grid, 256, 0, st>>>(x, R, C, q, e8);
+    if (x_is_bf16)
+        quant_mx_kernel<true><<<grid, 256, 0, st>>>(x, R, C, q, e8);
+    else
+        quant_mx_kernel<false><<<grid, 256, 0, st>>>(x, R, C, q, e8);
     return cudaGetLastError();
 }
 

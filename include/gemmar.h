@@ -83,11 +83,11 @@ enum { GEMMAR_SCALE_BLOCK128 = 0, GEMMAR_SCALE_MX32 = 1, GEMMAR_SCALE_PTPC = 2 }
                                              reducer's bounded wait expires (GEMMAR_ERR_TIMEOUT) */
 #define GEMMAR_NO_SELF_TEST    (1u << 3)  /* create: skip the closed-form self-test */
 #define GEMMAR_CTA_PAIR        (1u << 5)  /* create: run blockscale GEMMs with N % 256 == 0 on the CTA-pair
-                                             kernel (256 x 256 tiles over two SMs, band partials parked in
-                                             shared memory and sent by bulk async copies) instead of the
-                                             one-CTA kernel; the same bits (tests); on the wo_b
-                                             band path slower (its GEMM ~2040 us against ~1780), and
-                                             without the in-kernel band reduce */
+                                             kernel (256 x 256 tiles over two SMs; band partials parked in
+                                             shared memory and copied out by two store warps) instead of
+                                             the one-CTA kernel; the same bits (tests); on the wo_b band
+                                             path its GEMM runs ~1810 us against ~1770 for the one-CTA
+                                             kernel, without the in-kernel band reduce */
 #define GEMMAR_FUSE_SLICES     (1u << 4)  /* fused: each output tile accumulates all P slices itself (no
                                              partials, no band reduce); see fused_gemm_reduce */
 #define GEMMAR_FUSE_ONCHIP     (1u << 6)  /* fused: the P slice partials of a tile stay on chip and are
@@ -255,23 +255,26 @@ int rowdequant_e4m3(gemmar_ctx *ctx, const uint8_t *q, const float *row_scale, i
 /*
  * quant_blockscale_e4m3 -- device quantiser for blockscale operands: groups
  * of group_rows x 128 (group_rows 1 for activations, 128 for weights) of an
- * fp32 [R,C] matrix; s = fp32(amax/448), q = e4m3_rn_sat(fp32(x/s)); a zero
- * group gives s = 0 and +0 codes.  The real call site quantises wo_b's bf16
- * input itself (sglang pull request #43480, "Numerics, measured where the
- * path engages").  q: uint8 [R,C]; scales: fp32 [ceil(R/group_rows), C/128].
+ * [R,C] matrix x of x_dtype (GEMMAR_DTYPE_BF16 or GEMMAR_DTYPE_F32; bf16 is
+ * widened to fp32 exactly); s = fp32(amax/448), q = e4m3_rn_sat(fp32(x/s));
+ * a zero group gives s = 0 and +0 codes.  The real call site quantises wo_b's
+ * bf16 input itself (sglang pull request #43480, "Numerics, measured where
+ * the path engages"), so bf16 is the input the layer sees.
+ * q: uint8 [R,C]; scales: fp32 [ceil(R/group_rows), C/128].
  * C % 128 == 0.  Bit-exact against the definition.
  */
-int quant_blockscale_e4m3(gemmar_ctx *ctx, const float *x, int64_t R, int64_t C, int group_rows,
+int quant_blockscale_e4m3(gemmar_ctx *ctx, const void *x, int x_dtype, int64_t R, int64_t C, int group_rows,
                           uint8_t *q, float *scales, void *stream);
 
 /*
- * quant_mx_e4m3 -- device mxfp8 quantiser: per 1x32 group of an fp32 [R,C]
- * matrix, byte = ceil(log2(fp32(amax/448))) + 127 from the IEEE bits (exact at
- * powers of two; sglang pull request #43480, review item 7), clamped to
- * [0,254], 0 for a zero group; q = e4m3_rn_sat(fp32(x * 2^(127-byte))).
+ * quant_mx_e4m3 -- device mxfp8 quantiser: per 1x32 group of an [R,C] matrix x
+ * of x_dtype (GEMMAR_DTYPE_BF16 or GEMMAR_DTYPE_F32), byte =
+ * ceil(log2(fp32(amax/448))) + 127 from the IEEE bits (exact at powers of two;
+ * sglang pull request #43480, review item 7), clamped to [0,254], 0 for a
+ * zero group; q = e4m3_rn_sat(fp32(x * 2^(127-byte))).
  * q: uint8 [R,C]; e8m0: uint8 [R, C/32].  C % 32 == 0.  Bit-exact.
  */
-int quant_mx_e4m3(gemmar_ctx *ctx, const float *x, int64_t R, int64_t C, uint8_t *q,
+int quant_mx_e4m3(gemmar_ctx *ctx, const void *x, int x_dtype, int64_t R, int64_t C, uint8_t *q,
                   uint8_t *e8m0, void *stream);
 
 /*
@@ -362,14 +365,33 @@ int fused_gemm_reduce(gemmar_ctx *ctx, int P, const uint8_t *const *A, const voi
  * the last call's contents; the call clears its counters and status word
  * itself.  Calls whose work overlaps on the GPU (different streams without an
  * ordering between them, or several host threads) race on the scratch and
- * give wrong results: keep them stream-ordered.  There is no status read-back:
- * a device-side wait that expires (possible only if the GEMM launch itself
- * failed) leaves `out` incomplete.
+ * give wrong results: keep them stream-ordered.
+ *
+ * Device-side failures: every wait inside the kernels is bounded (2 s).  If
+ * one expires -- for instance a GEMM CTA whose operand loads or tensor-core
+ * work stall that long on a GPU shared with other work -- the kernels stop
+ * early, the call has still returned GEMMAR_OK (it returns before the work
+ * runs), and `out` is left incomplete.  The failure is recorded in the
+ * scratch's status word: read it with fused_gemm_reduce_noalloc_status after
+ * the call's work has completed, before the next call on that device clears
+ * it.
  */
 #define GEMMAR_NOALLOC_MAX_PARTIALS (8 * 1024 * 1024)
 int fused_gemm_reduce_noalloc(int P, const uint8_t *const *A, const float *const *sa,
                               const uint8_t *const *B, const float *const *sb,
                               int64_t M, int64_t N, int64_t K, int bands, uint16_t *out, void *stream);
+
+/*
+ * fused_gemm_reduce_noalloc_status -- the device status of the last
+ * fused_gemm_reduce_noalloc call on the current device: GEMMAR_OK, or
+ * GEMMAR_ERR_TIMEOUT when a bounded wait of its kernels expired (then its
+ * `out` is incomplete), with *detail (if not NULL) set to the wait site.
+ * Reads the 8-byte status word with a synchronous device-to-host copy (no
+ * allocation): call it after that call's work has completed (for example
+ * after synchronising its stream).  GEMMAR_ERR_DEVICE if the current device
+ * has made no such call yet.  The pages have no counterpart.
+ */
+int fused_gemm_reduce_noalloc_status(int *detail);
 
 #ifdef __cplusplus
 }

@@ -108,31 +108,61 @@ def test_rowdequant_all_codes(g, ctx):
 
 # ---------------------------------------------------------------- quantisers
 
-@pytest.mark.parametrize("R,C,gr", [(256, 512, 1), (77, 384, 1), (256, 512, 128), (300, 256, 128)])
-def test_quant_blockscale_bitexact(g, ctx, R, C, gr):
+def _as_input(x, dtype):
+    """The quantiser's device input of dtype, and its exact fp32 value (bf16
+    widens to fp32 exactly) for the oracle."""
+    xt = torch.from_numpy(np.ascontiguousarray(x))
+    if dtype == "bf16":
+        xt = xt.to(torch.bfloat16)
+    return xt.cuda(), xt.float().numpy()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("R,C,gr", [(256, 512, 1), (77, 384, 1), (3, 128, 1), (256, 512, 128), (300, 256, 128),
+                                    (5, 384, 128)])
+def test_quant_blockscale_bitexact(g, ctx, R, C, gr, dtype):
     x = synthetic.normal(3, synthetic.TID_A, R, (R, C), sigma=0.02 if gr == 128 else 1.0)
     x[0, :128] = 0.0
+    x[-1, -128:] = np.float32(448.0 * 2.0 ** -7)     # a group whose amax is a power of two of 448
+    xd, xw = _as_input(x, dtype)
     q = torch.empty((R, C), dtype=torch.uint8, device="cuda")
     s = torch.empty(((R + gr - 1) // gr, C // 128), dtype=torch.float32, device="cuda")
-    g.quant_blockscale_e4m3(ctx, dev(x), gr, q, s)
+    g.quant_blockscale_e4m3(ctx, xd, gr, q, s)
     torch.cuda.synchronize()
-    q_ref, s_ref = oracle.quant_block(x, gr, 128)
+    q_ref, s_ref = oracle.quant_block(xw, gr, 128)
     assert np.array_equal(s.cpu().numpy(), s_ref)
     assert np.array_equal(q.cpu().numpy(), q_ref)
 
 
-@pytest.mark.parametrize("R,C", [(128, 256), (37, 96)])
-def test_quant_mx_bitexact(g, ctx, R, C):
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("R,C", [(128, 256), (37, 96), (3, 32)])
+def test_quant_mx_bitexact(g, ctx, R, C, dtype):
     x = synthetic.normal(4, synthetic.TID_A, R, (R, C))
-    x[1, 32:64] = 0.0
-    x[2, 0:32] = np.float32(448.0 * 2.0 ** -5)       # a group on an exact power of two of 448
-    x[3, 64:96] *= np.float32(2.0 ** -100)
+    x[1 % R, 0:32] = 0.0
+    x[2 % R, C - 32:C] = np.float32(448.0 * 2.0 ** -5)       # a group on an exact power of two of 448
+    x[R - 1, 0:32] *= np.float32(2.0 ** -100)
+    xd, xw = _as_input(x, dtype)
     q = torch.empty((R, C), dtype=torch.uint8, device="cuda")
     e = torch.empty((R, C // 32), dtype=torch.uint8, device="cuda")
-    g.quant_mx_e4m3(ctx, dev(x), q, e)
+    g.quant_mx_e4m3(ctx, xd, q, e)
     torch.cuda.synchronize()
-    q_ref, e_ref = oracle.quant_mx(x)
+    q_ref, e_ref = oracle.quant_mx(xw)
     assert np.array_equal(e.cpu().numpy(), e_ref)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+
+
+def test_quant_blockscale_bf16_wo_b_activation(g, ctx):
+    """The call site's own case: wo_b's bf16 activations [4096, 2048] quantised
+    per 1x128 on the device, bit for bit against the oracle quantiser fed the
+    same rows."""
+    x = synthetic.normal(6, synthetic.TID_A, 0, (4096, 2048))
+    xd, xw = _as_input(x, "bf16")
+    q = torch.empty((4096, 2048), dtype=torch.uint8, device="cuda")
+    s = torch.empty((4096, 16), dtype=torch.float32, device="cuda")
+    g.quant_blockscale_e4m3(ctx, xd, 1, q, s)
+    torch.cuda.synchronize()
+    q_ref, s_ref = oracle.quant_act_1x128(xw)
+    assert np.array_equal(s.cpu().numpy(), s_ref)
     assert np.array_equal(q.cpu().numpy(), q_ref)
 
 
