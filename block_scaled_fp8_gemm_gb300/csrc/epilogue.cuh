@@ -141,12 +141,12 @@ __device__ __forceinline__ void signal_band(const GemmOut &o, int band, uint32_t
 struct BandSignals {
     int band = -1;
     uint32_t n = 0;
-    __device__ __forceinline__ void add(const GemmOut &o, int b)
+    __device__ __forceinline__ void add(const GemmOut &o, int b, uint32_t count = 1)
     {
         if (b != band)
             flush(o);
         band = b;
-        ++n;
+        n += count;
     }
     __device__ __forceinline__ void flush(const GemmOut &o)
     {

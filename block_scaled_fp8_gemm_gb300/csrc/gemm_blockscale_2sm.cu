@@ -10,19 +10,26 @@
 // K=32) reading both CTAs' stages.  Per SM that is the MMA shape of the
 // one-CTA 128 x 256 tile with half of its B traffic, which frees the shared
 // memory for what limits the one-CTA kernel on the band path: the tile's fp32
-// partial (128 KB per SM) is parked in shared memory at tile end and leaves
-// through one bulk asynchronous copy per warp while the next tile computes,
-// instead of stalling the epilogue on 128 KB of global stores.
+// partial (128 KB per SM) is parked in shared memory at tile end and two
+// store warps copy it to HBM with ordinary 16-byte stores while the next tile
+// computes, instead of stalling the epilogue on 128 KB of global stores.  (The
+// stores do not go through the TMA unit, which must keep issuing the next
+// stages' operand loads meanwhile.)
 //
 // Per CTA:
 //   warp 0       TMA producer: 3 stages of 16 KB A + 16 KB B
 //   warp 1       TMEM allocation (both CTAs); MMA issue (leader only: the
 //                whole warp runs the loop, lane 0 polls, one lane issues)
+//   warps 2-3    band path: park drain -- warp 2 + h copies the parks of the
+//                four epilogue warps of column half h to the blocked partials
+//                and publishes the band (batched per run of same-band tiles)
 //   warps 4-11   epilogue: thread = one row x 128 columns (2 TMEM loads of 64
 //                per K-step), promotion acc += (sa * sb) * P_kb, tile store
 // Barriers: stage-full counts both CTAs' TMA bytes on the leader; stage-empty
 // and TMEM-full are multicast-committed to both CTAs; TMEM-empty lives on the
-// leader and collects 8 local + 8 remote arrivals.
+// leader and collects 8 local + 8 remote arrivals; park-full / park-empty (one
+// pair per epilogue warp) hand each 16 KB park between its epilogue warp and
+// its store warp.
 #include <algorithm>
 
 #include "epilogue.cuh"
@@ -44,7 +51,7 @@ constexpr int kOffA = 0;
 constexpr int kOffB = kStages * kABytes;
 constexpr int kOffPark = kOffB + kStages * kBBytes;
 constexpr int kOffBar = kOffPark + kEpiWarps * kParkBytes;
-constexpr int kNumBars = 2 * kStages + 2 * kBufs + 1;
+constexpr int kNumBars = 2 * kStages + 2 * kBufs + 1 + 2 * kEpiWarps;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -90,21 +97,6 @@ __device__ __forceinline__ PairTile decode_pair(int t, const TileGrid &g)
     return c;
 }
 
-// Bulk asynchronous copy shared -> global (16-byte aligned, size % 16 == 0),
-// tracked in this thread's bulk groups.
-__device__ __forceinline__ void bulk_store(void *gdst, uint32_t ssrc, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Every bulk group of this thread complete (writes performed).
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// Generic-proxy shared-memory writes visible to the async proxy (bulk copies).
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-// Async-proxy global writes ordered before this thread's later generic accesses.
-__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-
 __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const __grid_constant__ BsParams prm)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -114,6 +106,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const 
     uint64_t *tfull = empty + kStages;     // [kBufs]
     uint64_t *tempty = tfull + kBufs;      // [kBufs], used on the leader
     uint64_t *final_bar = tempty + kBufs;
+    uint64_t *park_full = final_bar + 1;           // [kEpiWarps]
+    uint64_t *park_empty = park_full + kEpiWarps;  // [kEpiWarps]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
 
@@ -136,6 +130,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const 
             mbar_init(tempty + b, 2 * kEpiWarps);
         }
         mbar_init(final_bar, 1);
+        for (int w = 0; w < kEpiWarps; ++w) {
+            mbar_init(park_full + w, 1);
+            mbar_init(park_empty + w, 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -229,6 +227,49 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const 
             if (elect_one())
                 tc_commit_pair(final_bar, 3);
             __syncwarp();
+        } else if (warp >= 2 && prm.o.out_mode == OUT_PARTIAL_F32 && g.slice_loop != 2) {
+            // ------------------------------------------------ park drain (band path)
+            const int h = warp - 2;   // column half whose four epilogue warps this warp serves
+            BandSignals signals;
+            uint32_t pk = 0;          // parks of each of those warps drained so far
+            bool ok = true;
+            for (int t = cluster; t < g.num_tiles && ok; t += nclusters) {
+                const PairTile tc = decode_pair(t, g);
+                const int m_cta = tc.m0 + 128 * (int)rank;
+                if (m_cta < tc.band_end) {
+                    const TileCoord ct{tc.b, tc.p, m_cta, tc.n0, 0};
+                    float4 *tb = partial_tile_base(prm.o, g, ct, 256);
+                    for (int q = 0; q < 4 && ok; ++q) {
+                        const int ew = h * 4 + q;   // epilogue warp 4 + ew owns lane quarter q, half h
+                        if (!mbar_wait(park_full + ew, pk & 1, abort_flag, prm.status, prm.timeout_ns,
+                                       SITE_PARK_FULL)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t park = smem_u32(smem + kOffPark + ew * kParkBytes);
+                        float4 *dst = tb + ((q * 8 + h * 4) * 8) * 32 + lane;
+#pragma unroll 1
+                        for (int i = 0; i < kParkBytes / 512; i += 4) {
+                            uint4 v[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                v[u] = ld_shared_v4(park + (uint32_t)(((i + u) * 32 + lane) * 16));
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                __stcg(dst + (i + u) * 32, make_float4(__uint_as_float(v[u].x), __uint_as_float(v[u].y),
+                                                                       __uint_as_float(v[u].z), __uint_as_float(v[u].w)));
+                        }
+                        __syncwarp();   // every lane has read the park
+                        if (lane == 0)
+                            mbar_arrive(park_empty + ew);
+                    }
+                    ++pk;
+                }
+                if (ok)
+                    signals.add(prm.o, tc.b, 4);   // this tile's four parks of half h (or none past the band end)
+            }
+            if (ok)
+                signals.flush(prm.o);
         }
     } else {
         setmaxnreg_inc<kRegsHigh>();
@@ -242,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const 
         const uint32_t tempty_leader = mapa_shared(smem_u32(tempty), 0);
         const bool partial = prm.o.out_mode == OUT_PARTIAL_F32;
         const bool exact = g.slice_loop == 2;
-        int pend_band = -1;   // band of the partial whose bulk copy is in flight
+        uint32_t pk = 0;      // partials parked so far (park-full/empty phase)
         uint32_t kiter = 0;
         bool ok = true;
         const int nsl = g.slice_loop ? g.P : 1;
@@ -341,20 +382,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const 
             __syncwarp();   // every lane's last read of the running sum precedes the staging writes
             // -------- tile store
             if (partial) {
-                // The previous partial's copy has had a whole tile to land: wait for
-                // it (which also frees the park), then publish its band.
-                if (lane == 0) {
-                    bulk_wait_all();
-                    fence_proxy_async_global();
-                }
-                if (pend_band >= 0)
-                    signal_band(prm.o, pend_band);
-                __syncwarp();
-                pend_band = -1;
                 if (m_cta < tc.band_end) {
                     // park this warp's 32 rows x 128 columns in the blocked order of the
                     // partial layout (chunks h*4 .. h*4+3 of lane quarter q are 16 KB
-                    // contiguous in W), then one bulk copy takes it to HBM
+                    // contiguous in W) once its store warp has copied the previous one
+                    if (!mbar_wait(park_empty + ew, (pk & 1) ^ 1, abort_flag, prm.status, prm.timeout_ns,
+                                   SITE_PARK_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -364,19 +400,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const 
                                          make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]),
                                                     __float_as_uint(a[2]), __float_as_uint(a[3])));
                         }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        const TileCoord ct{tc.b, tc.p, m_cta, tc.n0, 0};
-                        float4 *tb = partial_tile_base(prm.o, g, ct, 256);
-                        bulk_store(tb + ((q * 8 + h * 4) * 8) * 32, park, (uint32_t)kParkBytes);
-                        bulk_commit();
-                    }
-                    pend_band = tc.b;
-                } else {
-                    // a CTA tile past the band end (ragged bands) owns no partial block
-                    signal_band(prm.o, tc.b);
+                    __syncwarp();   // every lane's park writes precede the arrive
+                    if (lane == 0)
+                        mbar_arrive(park_full + ew);
+                    ++pk;
                 }
+                // a CTA tile past the band end (ragged bands) owns no partial block: its
+                // store warp publishes the band without waiting for a park
             } else if (prm.o.out_mode == OUT_BF16) {
                 const TileCoord ct{tc.b, tc.p, m_cta, tc.n0, 0};
                 char *base = tile_out_base(prm.o, g, ct, 2) + ((int64_t)q * 32 * g.N + h * 128) * 2;
@@ -407,14 +437,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_2sm_kernel(const 
                 }
             }
         }
-        // the last partial: its copy completes before the band is published and
-        // before the shared memory it reads from is released
-        if (lane == 0) {
-            bulk_wait_all();
-            fence_proxy_async_global();
-        }
-        if (ok && pend_band >= 0)
-            signal_band(prm.o, pend_band);
     }
 
     __syncwarp();

@@ -87,6 +87,8 @@ enum WaitSite : int {
     SITE_TEARDOWN_MMA = 5,
     SITE_TEARDOWN_TMA = 6,
     SITE_REDUCE_BAND = 7,
+    SITE_PARK_FULL = 8,    // a store warp waiting for its epilogue warp's parked partial
+    SITE_PARK_EMPTY = 9,   // an epilogue warp waiting for its park to be copied out
 };
 
 constexpr int kErrTimeout = 6;   // == GEMMAR_ERR_TIMEOUT
