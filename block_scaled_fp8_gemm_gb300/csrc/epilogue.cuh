@@ -172,9 +172,12 @@ struct BandSignals {
 // the ring needs no warp barrier.  The arithmetic is that of the band reduce:
 // ((W_0 + W_1) + W_2) + ..., fp32, then bf16 RN.
 // ---------------------------------------------------------------------------
-constexpr int kReduceRingStages = 4;
-constexpr int kReduceWarpRingBytes = kReduceRingStages * kMaxP * 512;   // per reducer warp
-constexpr int kReduceRingBytes = 2 * kReduceWarpRingBytes;              // two reducer warps per CTA
+constexpr int kReduceRingStages = 4;   // default ring depth (items in flight per reducer warp)
+// shared-memory ring of one reducer warp with RS stages, and of the two reducer warps of a CTA
+template <int RS = kReduceRingStages>
+__host__ __device__ constexpr int reduce_warp_ring_bytes() { return RS * kMaxP * 512; }
+template <int RS = kReduceRingStages>
+__host__ __device__ constexpr int reduce_ring_bytes() { return 2 * reduce_warp_ring_bytes<RS>(); }
 
 struct BandClaim {
     int band = 0;                // lowest band that may still have unclaimed blocks
@@ -227,15 +230,19 @@ __device__ __forceinline__ int claim_retired_block(const GemmOut &o, const TileG
     return __shfl_sync(0xffffffffu, blk, 0);
 }
 
-// ring: shared address of kReduceWarpRingBytes (16-byte aligned) that nothing
+// ring: shared address of reduce_warp_ring_bytes<RS>() (16-byte aligned) that nothing
 // else uses while this reducer warp runs.  A block is read as eight items, one
 // 16-byte column unit (4 columns) of each lane's row from every slice (P x 512 B
 // per item, one ring stage).  Whole warp calls.
+template <int RS = kReduceRingStages>
 __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGrid &g, int bn, uint32_t ring,
                                                   const volatile int *epi_done, int epi_warps, uint64_t timeout_ns)
 {
     constexpr int IPB = 8;                     // items per block
     constexpr int STAGE = kMaxP * 512;         // bytes per ring stage
+    // the block of an item in flight is kept in one of two slots (even and odd
+    // groups of IPB items): the ring may run at most one group ahead
+    static_assert(RS >= 1 && RS <= IPB, "ring deeper than one block of items");
     const int lane = threadIdx.x & 31;
     const int P = g.P;
     const int nchunk = bn / 32;
@@ -251,7 +258,7 @@ __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGr
     bool more = true;
     int issued = 0;
     BandClaim cl;
-    // item k = column unit k % 8 of its block, in ring stage k % kReduceRingStages
+    // item k = column unit k % 8 of its block, in ring stage k % RS
     auto issue = [&](int k) {
         const int j = (k / IPB) & 1;
         if (more && k % IPB == 0) {
@@ -269,7 +276,7 @@ __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGr
             const int64_t i = r / (4 * nchunk);
             const float4 *src = W + ((int64_t)b * P * tiles_per_band + i) * tile_f4 +
                                 ((q * nchunk + c) * 8 + k % IPB) * 32 + lane;
-            const uint32_t dst = ring + (k % kReduceRingStages) * STAGE + lane * 16;
+            const uint32_t dst = ring + (k % RS) * STAGE + lane * 16;
             for (int p = 0; p < P; ++p)
                 ptx::cp_async_cg16(dst + p * 512, src + p * slice_f4);
             ++issued;
@@ -277,12 +284,12 @@ __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGr
         ptx::cp_async_commit();   // one group per item slot, empty past the last item
     };
 #pragma unroll 1
-    for (int k = 0; k < kReduceRingStages; ++k)
+    for (int k = 0; k < RS; ++k)
         issue(k);
 #pragma unroll 1
     for (int k = 0; k < issued; ++k) {
-        ptx::cp_async_wait<kReduceRingStages - 1>();   // this lane's copies of item k have landed
-        const uint32_t st = ring + (k % kReduceRingStages) * STAGE + lane * 16;
+        ptx::cp_async_wait<RS - 1>();   // this lane's copies of item k have landed
+        const uint32_t st = ring + (k % RS) * STAGE + lane * 16;
         const uint4 w = ptx::ld_shared_v4(st);
         float a[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z), __uint_as_float(w.w)};
         for (int p = 1; p < P; ++p) {
@@ -319,7 +326,7 @@ __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGr
                 reinterpret_cast<uint4 *>(dst)[1] = make_uint4(o4, o5, o6, o7);
             }
         }
-        issue(k + kReduceRingStages);   // reuses this item's stage: this lane has read it
+        issue(k + RS);   // reuses this item's stage: this lane has read it
     }
     ptx::cp_async_wait<0>();
 }

@@ -31,7 +31,11 @@ struct BsCfg {
     static constexpr int kBBytes = BN * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kEpiWarps = 8;
-    static constexpr int kStagingBytes = kEpiWarps * 4096;
+    static constexpr int kRingStages = kReduceRingStages;   // the band reducers' ring depth
+    // 4 KB per epilogue warp for staged C stores; on the band path the two band
+    // reducer warps use the same bytes as their ring
+    static constexpr int kStagingBytes = kEpiWarps * 4096 > reduce_ring_bytes<kRingStages>()
+                                             ? kEpiWarps * 4096 : reduce_ring_bytes<kRingStages>();
     static constexpr int kTmemCols = 2 * BN;
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kStages * kABytes;
@@ -42,7 +46,7 @@ struct BsCfg {
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kTmemCols <= 512, "TMEM budget");
-    static_assert(kStagingBytes >= kReduceRingBytes, "the band reducer's ring reuses the staging");
+    static_assert(kStagingBytes >= reduce_ring_bytes<kRingStages>(), "the band reducer's ring reuses the staging");
 };
 
 constexpr int kThreads = 384;
@@ -180,7 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
         } else if (warp >= 2 && prm.o.out_mode == OUT_PARTIAL_F32 && prm.o.reduce_next != nullptr) {
             // ------------------------------------------------ band reducers (the staging is
             // unused when the epilogue writes blocked partials): one half of it each
-            band_reducer_warp(prm.o, g, BN, smem_u32(smem + C::kOffStaging) + (warp - 2) * kReduceWarpRingBytes,
+            band_reducer_warp<C::kRingStages>(prm.o, g, BN,
+                                              smem_u32(smem + C::kOffStaging) + (warp - 2) * reduce_warp_ring_bytes<C::kRingStages>(),
                                  epi_done, C::kEpiWarps, prm.timeout_ns);
         }
     } else {

@@ -39,7 +39,11 @@ struct MxCfg {
     static constexpr int kSfBytes = PT ? 0 : 512 + 1024;
     static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
     static constexpr int kEpiWarps = 8;
-    static constexpr int kStagingBytes = kEpiWarps * 4096;
+    static constexpr int kRingStages = kReduceRingStages;   // the band reducers' ring depth
+    // 4 KB per epilogue warp for staged C stores; on the band path the two band
+    // reducer warps use the same bytes as their ring
+    static constexpr int kStagingBytes = kEpiWarps * 4096 > reduce_ring_bytes<kRingStages>()
+                                             ? kEpiWarps * 4096 : reduce_ring_bytes<kRingStages>();
     static constexpr int kTmemCols = 512;
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kStages * kABytes;
@@ -50,7 +54,7 @@ struct MxCfg {
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
     static_assert(kBBytes % 1024 == 0, "B tiles stay 1024-byte aligned");
-    static_assert(kStagingBytes >= kReduceRingBytes, "the band reducer's ring reuses the staging");
+    static_assert(kStagingBytes >= reduce_ring_bytes<kRingStages>(), "the band reducer's ring reuses the staging");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(PT ? 2 * BN <= 512 : 2 * BN <= (int)kSfaCol, "accumulators below the scale columns");
 };
@@ -254,7 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
       } else if (prm.o.out_mode == OUT_PARTIAL_F32 && prm.o.reduce_next != nullptr) {
             // ------------------------------------------------ band reducers (warps 2-3; the
             // staging is unused when the epilogue writes blocked partials): half of it each
-            band_reducer_warp(prm.o, g, BN, smem_u32(smem + C::kOffStaging) + (warp - 2) * kReduceWarpRingBytes,
+            band_reducer_warp<C::kRingStages>(prm.o, g, BN,
+                                              smem_u32(smem + C::kOffStaging) + (warp - 2) * reduce_warp_ring_bytes<C::kRingStages>(),
                                  epi_done, C::kEpiWarps, prm.timeout_ns);
       }
     } else {
