@@ -60,6 +60,9 @@ struct MxCfg {
 };
 
 constexpr int kThreads = 384;
+// Band path: pause between a warp's partial-store chunks (4 KB per warp), so a
+// tile's partial leaves over the next tile's compute rather than in one burst.
+constexpr unsigned kStorePaceNs = 600;
 constexpr int kRegsLow = 56;    // warpgroup 0 (producer, MMA) after setmaxnreg.dec
 constexpr int kRegsHigh = 224;  // warpgroups 1-2 (epilogue) after setmaxnreg.inc
 
@@ -420,6 +423,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
             const int rows_valid = max(0, min(32, tc.valid_rows - q * 32));
             const int esz = prm.o.out_mode == OUT_BF16 ? 2 : 4;
             char *base = tile_out_base(prm.o, g, tc, esz) + (int64_t)q * 32 * g.N * esz;
+            if (!PT && prm.o.out_mode == OUT_PARTIAL_F32) {
+                // mx band path: read the warp's whole share of the tile (its 32-column chunks
+                // h, h+2, ...) out of TMEM first and hand the buffer back, then store the fp32
+                // partial one chunk at a time with a pause between chunks.  The next tile's
+                // MMAs run meanwhile; spreading the 112-128 KB of partial stores over that
+                // time instead of sending them in one burst keeps the SM's memory path free
+                // for the operand loads the tensor cores wait on.
+                constexpr int NW = (NCH + 1) / 2;   // chunks per warp
+                uint32_t r[NW][32];
+#pragma unroll
+                for (int j = 0; j < NW; ++j)
+                    if (h + 2 * j < NCH)
+                        tmem_ld_x32(lane_base + buf * BN + (h + 2 * j) * 32, r[j]);
+#pragma unroll
+                for (int j = 0; j < NW; ++j)
+                    tmem_wait_ld(r[j]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(tempty + buf);
+                float4 *tb = partial_tile_base(prm.o, g, tc, BN);
+#pragma unroll
+                for (int j = 0; j < NW; ++j) {
+                    if (h + 2 * j >= NCH)
+                        continue;
+                    if (j > 0)
+                        __nanosleep(kStorePaceNs);
+                    store_partial_chunk<BN>(tb, q, h + 2 * j, reinterpret_cast<const float *>(r[j]));
+                }
+                signals.add(prm.o, tc.b);
+                ++titer;
+                continue;
+            }
             for (int c = h; c < NCH; c += 2) {
                 uint32_t r[32];
                 tmem_ld_x32(lane_base + buf * BN + c * 32, r);
