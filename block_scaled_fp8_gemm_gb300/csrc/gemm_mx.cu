@@ -423,8 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
             const int rows_valid = max(0, min(32, tc.valid_rows - q * 32));
             const int esz = prm.o.out_mode == OUT_BF16 ? 2 : 4;
             char *base = tile_out_base(prm.o, g, tc, esz) + (int64_t)q * 32 * g.N * esz;
-            if (!PT && prm.o.out_mode == OUT_PARTIAL_F32) {
-                // mx band path: read the warp's whole share of the tile (its 32-column chunks
+            if (prm.o.out_mode == OUT_PARTIAL_F32) {
+                // Band path: read the warp's whole share of the tile (its 32-column chunks
                 // h, h+2, ...) out of TMEM first and hand the buffer back, then store the fp32
                 // partial one chunk at a time with a pause between chunks.  The next tile's
                 // MMAs run meanwhile; spreading the 112-128 KB of partial stores over that
@@ -443,6 +443,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(tempty + buf);
+                if constexpr (PT) {
+                    // ptpc: the per-token x per-channel scale, chunk by chunk (the empty asm
+                    // keeps the compiler from hoisting every chunk's scale broadcasts at once)
+#pragma unroll
+                    for (int j = 0; j < NW; ++j) {
+                        if (h + 2 * j < NCH) {
+                            ptpc_scale16(r[j], sa_m, sb_mine, j * 8);
+                            ptpc_scale16(r[j] + 16, sa_m, sb_mine, j * 8 + 4);
+                        }
+                        asm volatile("" ::: "memory");
+                    }
+                }
                 float4 *tb = partial_tile_base(prm.o, g, tc, BN);
 #pragma unroll
                 for (int j = 0; j < NW; ++j) {

@@ -561,38 +561,74 @@ __device__ __forceinline__ float segment_max(float m)
     return m;
 }
 
-// 1x128: an aligned segment of 128/V lanes per (row, 128-group); a warp covers
-// 32V/128 groups per step and takes two steps at once (loads in flight).
+// 1x128: eight lanes per (row, 128-group), 16 values per lane (two 16-byte
+// loads of bf16 or four of fp32), so a warp step covers four groups and the
+// per-group scale arithmetic (an IEEE division and reciprocal) is shared by
+// four groups' worth of values.  With C % 128 == 0 group gi = row * (C/128) + g
+// starts at element 128 * gi, so the groups are walked as one flat sequence.
+constexpr int kQSteps = 2;    // warp steps with loads in flight together
+
 template <bool BF16>
-__global__ void __launch_bounds__(256) quant_1x128_kernel(const void *__restrict__ x, int64_t R, int64_t C,
+struct Lane16x {
+    static constexpr int NL = BF16 ? 2 : 4;   // 16-byte loads per lane
+    Lane16<BF16> part[NL];
+    __device__ __forceinline__ void load(const void *x, int64_t e)
+    {
+#pragma unroll
+        for (int i = 0; i < NL; ++i)
+            part[i].load(x, e + i * Lane16<BF16>::V);
+    }
+    __device__ __forceinline__ float amax() const
+    {
+        float m = part[0].amax();
+#pragma unroll
+        for (int i = 1; i < NL; ++i)
+            m = fmaxf(m, part[i].amax());
+        return m;
+    }
+    __device__ __forceinline__ void store_codes(uint8_t *q, int64_t e, const Enc &enc) const
+    {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < NL; ++i) {
+            const float *v = part[i].v;
+            if constexpr (BF16) {
+                w[2 * i] = enc(v[0], v[1], v[2], v[3]);
+                w[2 * i + 1] = enc(v[4], v[5], v[6], v[7]);
+            } else {
+                w[i] = enc(v[0], v[1], v[2], v[3]);
+            }
+        }
+        *reinterpret_cast<uint4 *>(q + e) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) quant_1x128_kernel(const void *__restrict__ x, int64_t ngroups,
                                                           uint8_t *__restrict__ q, float *__restrict__ scales)
 {
-    using L16 = Lane16<BF16>;
-    constexpr int L = 128 / L16::V;   // lanes per group
-    constexpr int GPW = 32 / L;       // groups per warp step
+    constexpr int L = 8;          // lanes per group
+    constexpr int GPW = 32 / L;   // groups per warp step
     const int lane = threadIdx.x & 31;
-    const int64_t G = C / 128;
-    const int64_t ngroups = R * G;
     const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int64_t w0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    for (int64_t step = w0 * 2; step * GPW < ngroups; step += warps_total * 2) {
-        int64_t gi[2], e[2];
-        L16 d[2];
+    for (int64_t step = w0 * kQSteps; step * GPW < ngroups; step += warps_total * kQSteps) {
+        int64_t gi[kQSteps];
+        Lane16x<BF16> d[kQSteps];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < kQSteps; ++u) {
             gi[u] = (step + u) * GPW + lane / L;
-            e[u] = (gi[u] / G) * C + (gi[u] % G) * 128 + (lane % L) * L16::V;
             if (gi[u] < ngroups)
-                d[u].load(x, e[u]);
+                d[u].load(x, gi[u] * 128 + (lane % L) * 16);
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < kQSteps; ++u) {
             const float m = segment_max<L>(gi[u] < ngroups ? d[u].amax() : 0.0f);
             if (gi[u] < ngroups) {
                 const float sc = __fdiv_rn(m, 448.0f);
                 if (lane % L == 0)
                     scales[gi[u]] = sc;
-                d[u].store_codes(q, e[u], Enc(sc));
+                d[u].store_codes(q, gi[u] * 128 + (lane % L) * 16, Enc(sc));
             }
         }
     }
@@ -895,13 +931,14 @@ cudaError_t launch_quant_blockscale(const void *x, int x_is_bf16, int64_t R, int
                                     float *scales, int num_sms, cudaStream_t st)
 {
     if (group_rows == 1) {
-        const int64_t gpw = x_is_bf16 ? 2 : 1;   // groups per warp step; two steps per pass
-        const int64_t need = (R * (C / 128) + 16 * gpw - 1) / (16 * gpw);
+        const int64_t ngroups = R * (C / 128);
+        const int64_t per_cta = 8 * 4 * kQSteps;   // 8 warps, 4 groups per warp step
+        const int64_t need = (ngroups + per_cta - 1) / per_cta;
         const int grid = (int)max64(1, min64(need, (int64_t)num_sms * 8));
         if (x_is_bf16)
-            quant_1x128_kernel<true><<<grid, 256, 0, st>>>(x, R, C, q, scales);
+            quant_1x128_kernel<true><<<grid, 256, 0, st>>>(x, ngroups, q, scales);
         else
-            quant_1x128_kernel<false><<<grid, 256, 0, st>>>(x, R, C, q, scales);
+            quant_1x128_kernel<false><<<grid, 256, 0, st>>>(x, ngroups, q, scales);
     } else {
         const int64_t nblk = ((R + 127) / 128) * (C / 128);
         const int grid = (int)max64(1, min64(nblk, (int64_t)num_sms * 8));

@@ -121,6 +121,32 @@ def test_fused_mx_vs_oracle(g, ctx, P, M, N, K, bands):
     check_bf16_output(out.float().cpu().numpy(), ref, f"fused mx P={P} M={M} N={N} K={K}")
 
 
+@pytest.mark.parametrize("K", [640, 768, 1152])
+def test_mx_scale_groups_with_a_partial_group(g, K):
+    """The mx kernel loads and copies the scale images of four K-blocks (4 x 128
+    of K) at a time; K/128 = 5, 6 or 9 leaves a last group of 1, 2 or 1 blocks.
+    Single GEMM against the oracle, the band path against the oracle, and the
+    on-chip sums bit-equal to the band path."""
+    P, M, N, bands = 3, 384, 448, 3
+    c = g.gemmar_create(0, M, N, K, P, flags=g.GEMMAR_NO_SELF_TEST, wait_timeout_ns=1_000_000_000)
+    try:
+        A, ea, B, eb = mx_operands(P, M, N, K, seed=K + 3)
+        one, _ = oracle.gemm_reduce(A[:1], ea[:1], B[:1], eb[:1], 1)
+        C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        g.gemm_mxfp8(c, dev(A[0]), dev(ea[0]), dev(B[0]), dev(eb[0]), C)
+        status_ok(g, c)
+        check_f32_output(C.cpu().numpy(), one, f"mx f32 {M}x{N}x{K}")
+        ref, _ = oracle.gemm_reduce(A, ea, B, eb, 1)
+        band = run_fused(g, c, A, ea, B, eb, g.GEMMAR_SCALE_MX32, bands, flags=g.GEMMAR_DEBUG_CANARY)
+        check_bf16_output(band.float().cpu().numpy(), ref, f"fused mx P={P} M={M} N={N} K={K}")
+        onchip = run_fused(g, c, A, ea, B, eb, g.GEMMAR_SCALE_MX32, bands, flags=g.GEMMAR_FUSE_ONCHIP)
+        assert torch.equal(onchip.view(torch.int16), band.view(torch.int16))
+        slices = run_fused(g, c, A, ea, B, eb, g.GEMMAR_SCALE_MX32, bands, flags=g.GEMMAR_FUSE_SLICES)
+        check_bf16_output(slices.float().cpu().numpy(), ref, f"mx slice loop K={K}")
+    finally:
+        c.close()
+
+
 @pytest.mark.parametrize("kind", [0, 1])
 def test_fused_equals_split_bitwise_and_is_deterministic(g, ctx, kind):
     P, M, N, K, bands = 4, 512, 512, 256, 4
