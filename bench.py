@@ -774,8 +774,9 @@ def run_ours(args, rank, world, local_rank):
 def run_profile_case(args):
     """One warm-up and one measured call of a single configuration, for
     profilers (ncu -k ... -s 1 -c 1): the fused layer (blockscale or ptpc P=8,
-    mx P=4, at M rows, with --flags), or the row codec alone on a [M, 7168]
-    bf16 matrix (--codec).  No timing is printed (only, for the fused layer, the
+    mx P=4, at M rows, with --flags), the row codec alone on a [M, 7168]
+    bf16 matrix (--codec), or the 1x128 activation quantiser alone on a
+    [M, 2048] bf16 matrix (--quant).  No timing is printed (only, for the fused layer, the
     share of blocks reduced during the GEMM); the exit status is the device status."""
     import torch
     import block_scaled_fp8_gemm_gb300 as g
@@ -784,8 +785,20 @@ def run_profile_case(args):
     M, N, K = args.m, N_HEAD, K_HEAD
     kind = {"blockscale": 0, "mx": 1, "ptpc": 2}[args.kind]
     P = 4 if kind == 1 else P_HEAD
-    ctx = g.gemmar_create(0, M, N, K, P, flags=g.GEMMAR_NO_SELF_TEST)
-    if args.codec:
+    # the codec and quantiser cases need no workspace: a minimal context keeps the
+    # device footprint (which a profiler saves and restores between passes) small
+    small = args.quant or args.codec
+    ctx = g.gemmar_create(0, 128 if small else M, 128 if small else N, 128 if small else K, 1 if small else P,
+                          flags=g.GEMMAR_NO_SELF_TEST)
+    if args.quant:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(0)
+        x = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
+        q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        s = torch.empty((M, K // 128), dtype=torch.float32, device=dev)
+        for _ in range(2):
+            g.quant_blockscale_e4m3(ctx, x, 1, q, s)
+    elif args.codec:
         gen = torch.Generator(device=dev)
         gen.manual_seed(0)
         x = torch.randn((M, N), generator=gen, device=dev).to(torch.bfloat16)
@@ -802,7 +815,7 @@ def run_profile_case(args):
             g.fused_gemm_reduce(ctx, A, sa, B, sb, out, scale_kind=kind, bands=P, flags=args.flags)
     torch.cuda.synchronize()
     code, detail = g.gemmar_status(ctx)
-    if not args.codec:
+    if not (args.codec or args.quant):
         ov, tot = g.gemmar_overlap_stats(ctx)
         print(f"blocks reduced during the GEMM: {ov} of {tot}", flush=True)
     ctx.close()
@@ -822,6 +835,8 @@ def main():
     ap.add_argument("--m", type=int, default=2048)
     ap.add_argument("--flags", type=int, default=0, help="fused_gemm_reduce flags (1 fp8 wire, 16 slice loop)")
     ap.add_argument("--codec", action="store_true", help="profile case: the row codec alone on [M, 7168] bf16")
+    ap.add_argument("--quant", action="store_true",
+                    help="profile case: the 1x128 activation quantiser alone on [M, 2048] bf16")
     args = ap.parse_args()
     if args.profile_case:
         return run_profile_case(args)

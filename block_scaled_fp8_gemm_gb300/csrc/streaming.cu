@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(256) band_reduce_kernel(const float *__restric
 // ones before it having been reduced by the GEMM kernel's reducer warps.
 // --------------------------------------------------------------------------
 template <int P>
-__global__ void __launch_bounds__(256) band_reduce_blocked_kernel(const float4 *__restrict__ W,
+__global__ void __launch_bounds__(256, 2) band_reduce_blocked_kernel(const float4 *__restrict__ W,
                                                                   uint16_t *__restrict__ out, int M, int N,
                                                                   int bands, int rows_per_band, int mt_per_band,
                                                                   int ntiles_n, int bn, const uint32_t *band_done,
@@ -149,12 +149,23 @@ __global__ void __launch_bounds__(256) band_reduce_blocked_kernel(const float4 *
             // float4 index of (band b, slice 0, tile i, q, c, unit 0, lane)
             const float4 *src = W + ((int64_t)b * P * tiles_per_band + i) * tile_f4 + ((q * nchunk + c) * 8) * 32 + lane;
             uint32_t o[16];
+            // the next item's P loads are issued before this item is summed: two items
+            // (2P 16-byte loads per lane) in flight keep HBM busy at two CTAs per SM
+            float4 nx[P];
+#pragma unroll
+            for (int p = 0; p < P; ++p)
+                nx[p] = __ldcs(src + (int64_t)p * tiles_per_band * tile_f4);
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 float4 v[P];
 #pragma unroll
                 for (int p = 0; p < P; ++p)
-                    v[p] = __ldcs(src + (int64_t)p * tiles_per_band * tile_f4 + u * 32);
+                    v[p] = nx[p];
+                if (u + 1 < 8) {
+#pragma unroll
+                    for (int p = 0; p < P; ++p)
+                        nx[p] = __ldcs(src + (int64_t)p * tiles_per_band * tile_f4 + (u + 1) * 32);
+                }
                 float4 a = v[0];
 #pragma unroll
                 for (int p = 1; p < P; ++p) {
@@ -563,14 +574,18 @@ __device__ __forceinline__ float segment_max(float m)
 
 // 1x128: eight lanes per (row, 128-group), 16 values per lane (two 16-byte
 // loads of bf16 or four of fp32), so a warp step covers four groups and the
-// per-group scale arithmetic (an IEEE division and reciprocal) is shared by
-// four groups' worth of values.  With C % 128 == 0 group gi = row * (C/128) + g
-// starts at element 128 * gi, so the groups are walked as one flat sequence.
+// per-group scale arithmetic (an IEEE division and reciprocal, executed by
+// every lane of the group) is spread over 16 values per lane.  (Four lanes of
+// 32 values halve that share but need 93 registers, two CTAs per SM, and ran
+// slower.)  With C % 128 == 0 group gi = row * (C/128) + g starts at element
+// 128 * gi, so the groups are walked as one flat sequence.
 constexpr int kQSteps = 2;    // warp steps with loads in flight together
+constexpr int kQLanes = 8;    // lanes per group
+constexpr int kQVals = 128 / kQLanes;
 
 template <bool BF16>
 struct Lane16x {
-    static constexpr int NL = BF16 ? 2 : 4;   // 16-byte loads per lane
+    static constexpr int NL = kQVals / Lane16<BF16>::V;   // 16-byte loads per lane
     Lane16<BF16> part[NL];
     __device__ __forceinline__ void load(const void *x, int64_t e)
     {
@@ -588,7 +603,7 @@ struct Lane16x {
     }
     __device__ __forceinline__ void store_codes(uint8_t *q, int64_t e, const Enc &enc) const
     {
-        uint32_t w[4];
+        uint32_t w[kQVals / 4];
 #pragma unroll
         for (int i = 0; i < NL; ++i) {
             const float *v = part[i].v;
@@ -599,7 +614,9 @@ struct Lane16x {
                 w[i] = enc(v[0], v[1], v[2], v[3]);
             }
         }
-        *reinterpret_cast<uint4 *>(q + e) = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int i = 0; i < kQVals / 16; ++i)
+            *reinterpret_cast<uint4 *>(q + e + 16 * i) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
     }
 };
 
@@ -607,7 +624,7 @@ template <bool BF16>
 __global__ void __launch_bounds__(256) quant_1x128_kernel(const void *__restrict__ x, int64_t ngroups,
                                                           uint8_t *__restrict__ q, float *__restrict__ scales)
 {
-    constexpr int L = 8;          // lanes per group
+    constexpr int L = kQLanes;    // lanes per group
     constexpr int GPW = 32 / L;   // groups per warp step
     const int lane = threadIdx.x & 31;
     const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -619,7 +636,7 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const void *__restrict
         for (int u = 0; u < kQSteps; ++u) {
             gi[u] = (step + u) * GPW + lane / L;
             if (gi[u] < ngroups)
-                d[u].load(x, gi[u] * 128 + (lane % L) * 16);
+                d[u].load(x, gi[u] * 128 + (lane % L) * kQVals);
         }
 #pragma unroll
         for (int u = 0; u < kQSteps; ++u) {
@@ -628,7 +645,7 @@ __global__ void __launch_bounds__(256) quant_1x128_kernel(const void *__restrict
                 const float sc = __fdiv_rn(m, 448.0f);
                 if (lane % L == 0)
                     scales[gi[u]] = sc;
-                d[u].store_codes(q, gi[u] * 128 + (lane % L) * 16, Enc(sc));
+                d[u].store_codes(q, gi[u] * 128 + (lane % L) * kQVals, Enc(sc));
             }
         }
     }
@@ -932,7 +949,7 @@ cudaError_t launch_quant_blockscale(const void *x, int x_is_bf16, int64_t R, int
 {
     if (group_rows == 1) {
         const int64_t ngroups = R * (C / 128);
-        const int64_t per_cta = 8 * 4 * kQSteps;   // 8 warps, 4 groups per warp step
+        const int64_t per_cta = 8 * (32 / kQLanes) * kQSteps;   // 8 warps, 32 / kQLanes groups per warp step
         const int64_t need = (ngroups + per_cta - 1) / per_cta;
         const int grid = (int)max64(1, min64(need, (int64_t)num_sms * 8));
         if (x_is_bf16)
