@@ -3,20 +3,28 @@
 // K-block granularity while draining TMEM ("MORI GEMM + All-Reduce
 // Benchmark", "Running the benchmark": A 1x128, B 128x128, fp32 scales).
 //
-// One persistent CTA per SM, 12 warps, warp-specialised:
+// One persistent CTA per SM, 16 warps, warp-specialised:
 //   warp 0      TMA producer: A tile 128x128 and B tile BNx128 (e4m3, 128-byte
 //               swizzle) per 128-K stage into a STAGES-deep shared ring.
 //   warp 1      MMA issuer: per stage, 4 x tcgen05.mma kind::f8f6f4
 //               (128 x BN x 32) into one of two TMEM accumulators, a fresh
 //               accumulation per K-block (the scale changes every K-block).
+//   warps 2-3   band path: band reducers (epilogue.cuh).
 //   warps 4-11  epilogue / scale promotion: each thread owns one tile row and
 //               BN/2 columns in registers and, per K-block, applies
 //               acc += (sa[m,kb] * sb[n/128,kb]) * P_kb as it drains TMEM,
 //               releasing the TMEM buffer back to the MMA warp as soon as it
 //               is read.  At tile end: bf16/fp32 store through shared staging,
-//               or the band-ordered fp32 partial plus a band counter signal.
+//               or, on the band path, the tile's sums written back into the
+//               TMEM buffer of its last K-block (a "park").
+//   warps 12-15 band path: store warps, one per TMEM lane quarter.  They copy a
+//               parked tile to the band-ordered fp32 partials, release the
+//               buffer and signal the band, while the epilogue warps promote
+//               the next tile -- 128 KB of stores per tile leave the SM at its
+//               store rate without holding the promotion.
 // TMEM holds 2 x BN fp32 columns (double-buffered K-blocks), so the tensor
-// cores run K-block kb+1 while the epilogue promotes kb.
+// cores run K-block kb+1 while the epilogue promotes kb.  On the band path the
+// first kParkLead K-blocks of a tile share the one buffer that is not parked.
 #include "epilogue.cuh"
 
 namespace gemmar {
@@ -41,7 +49,7 @@ struct BsCfg {
     static constexpr int kOffB = kStages * kABytes;
     static constexpr int kOffStaging = kOffB + kStages * kBBytes;
     static constexpr int kOffBar = kOffStaging + kStagingBytes;
-    static constexpr int kNumBars = 2 * kStages + 5;
+    static constexpr int kNumBars = 2 * kStages + 6;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -49,9 +57,48 @@ struct BsCfg {
     static_assert(kStagingBytes >= reduce_ring_bytes<kRingStages>(), "the band reducer's ring reuses the staging");
 };
 
-constexpr int kThreads = 384;
-constexpr int kRegsLow = 56;    // warpgroup 0 (producer, MMA) after setmaxnreg.dec
-constexpr int kRegsHigh = 224;  // warpgroups 1-2 (epilogue) after setmaxnreg.inc
+constexpr int kThreads = 512;
+constexpr int kRegsLow = 56;    // warpgroups 0 (producer, MMA, reducers) and 3 (store warps) after setmaxnreg.dec
+constexpr int kRegsHigh = 200;  // warpgroups 1-2 (epilogue) after setmaxnreg.inc
+constexpr int kRegsNeeded = 2 * 128 * kRegsLow + 256 * kRegsHigh;
+static_assert(kRegsNeeded <= 65536, "register split");
+constexpr int kStoreWarps = 4;
+// K-blocks at the start of a band-path tile that run in one TMEM buffer while
+// the store warps drain the previous tile's partial from the other.  Each of
+// them waits for its own promotion round trip (about 0.45 us more than a
+// double-buffered K-block), while 128 KB takes about 2 us to leave an SM; two
+// is the measured optimum at the wo_b shapes (serial band GEMM at P=8,
+// M=16384: lead 1 1744-1808 us, 2 1693-1718, 3 1718-1761, 5 1822-1835).
+constexpr int kParkLead = 2;
+
+// TMEM K-block buffer of each K-step; the MMA, epilogue and store warps step
+// through the same sequence.  Without a park the two buffers alternate.  With
+// one, the buffer of a tile's last K-step holds the tile's partial until the
+// store warps have read it: the next tile's first kParkLead K-steps (at most
+// all but its last) use the other buffer, then the two alternate again,
+// starting with the parked one.
+struct BufSeq {
+    uint32_t use0 = 0, use1 = 0;   // K-steps given to each buffer so far (registers, not an array)
+    int last = 1;                  // buffer of the previous tile's last K-step
+    // buffer of K-step ks (of nks) of the current tile; n = its use index
+    __device__ __forceinline__ int next(int ks, int nks, bool park, uint32_t &n)
+    {
+        // the tile's last K-step always reuses the parked buffer (lead <= nks - 1), so a
+        // tile cannot be parked before the store warps have taken the previous one
+        const int lead = min(kParkLead, nks - 1);
+        int b;
+        if (!park)
+            b = (int)((use0 + use1) & 1u);
+        else
+            b = ks < lead ? 1 - last : last ^ ((ks - lead) & 1);
+        n = b ? use1 : use0;
+        use0 += b ? 0u : 1u;
+        use1 += b ? 1u : 0u;
+        if (ks == nks - 1)
+            last = b;
+        return b;
+    }
+};
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __grid_constant__ BsParams prm)
@@ -64,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
     uint64_t *tfull = empty + C::kStages;   // [2]
     uint64_t *tempty = tfull + 2;           // [2]
     uint64_t *final_bar = tempty + 2;
+    uint64_t *park_full = final_bar + 1;    // a tile's partial is in TMEM (8 epilogue warps arrive)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
     volatile int *epi_done = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 8);   // epilogue warps finished
@@ -73,6 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
     const TileGrid &g = prm.g;
     const int KB = g.K / 128;
     const int NKS = (g.slice_loop ? g.P : 1) * KB;   // K-blocks per tile
+    const bool park = prm.o.out_mode == OUT_PARTIAL_F32;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -84,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
             mbar_init(tempty + b, C::kEpiWarps);
         }
         mbar_init(final_bar, 1);
+        mbar_init(park_full, C::kEpiWarps);
         *abort_flag = 0;
         *epi_done = 0;
         fence_mbar_init();
@@ -145,12 +195,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
             // ------------------------------------------------ MMA issuer
             const uint32_t idesc = idesc_f8_e4m3(128, BN);
             int stage = 0;
-            uint32_t ph = 0, kiter = 0;
+            uint32_t ph = 0;
+            BufSeq seq;
             bool ok = true;
             for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
                 for (int ks = 0; ks < NKS; ++ks) {
-                    const uint32_t buf = kiter & 1, tph = (kiter >> 1) & 1;
-                    if (!mbar_wait(tempty + buf, tph ^ 1, abort_flag, prm.status, prm.timeout_ns,
+                    uint32_t n;
+                    const int buf = seq.next(ks, NKS, park, n);
+                    if (!mbar_wait(tempty + buf, (n & 1) ^ 1, abort_flag, prm.status, prm.timeout_ns,
                                    SITE_MMA_TMEM_EMPTY) ||
                         !mbar_wait(full + stage, ph, abort_flag, prm.status, prm.timeout_ns, SITE_MMA_FULL)) {
                         ok = false;
@@ -165,7 +217,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
                         mma_f8(d, ad + 2 * k, bd + 2 * k, idesc, k > 0 ? 1u : 0u);
                     tc_commit(empty + stage);   // stage reusable once these MMAs have read it
                     tc_commit(tfull + buf);     // K-block partial ready for promotion
-                    ++kiter;
                     if (++stage == C::kStages) {
                         stage = 0;
                         ph ^= 1;
@@ -186,9 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
             // unused when the epilogue writes blocked partials): one half of it each
             band_reducer_warp<C::kRingStages>(prm.o, g, BN,
                                               smem_u32(smem + C::kOffStaging) + (warp - 2) * reduce_warp_ring_bytes<C::kRingStages>(),
-                                 epi_done, C::kEpiWarps, prm.timeout_ns);
+                                 epi_done, C::kEpiWarps + kStoreWarps, prm.timeout_ns);
         }
-    } else {
+    } else if (warp < 12) {
         setmaxnreg_inc<kRegsHigh>();
         // ---------------------------------------------------- epilogue
         constexpr int HALF = BN / 2;
@@ -200,10 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
         const int row = q * 32 + lane;  // tile row owned by this thread
         const uint32_t staging = smem_u32(smem + C::kOffStaging + ew * 4096);
         const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + h * HALF;
-        uint32_t kiter = 0;
+        BufSeq seq;
         bool ok = true;
         const int nsl = g.slice_loop ? g.P : 1;
-        BandSignals signals;
         for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
             const TileCoord tc = decode_tile<BN>(t, g);
             const int64_t mrow = min(tc.m0 + row, g.M - 1);
@@ -231,35 +281,59 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
                     a_next = __ldg(sa_row + kb);
                     b_next = __ldg(sb_blk + kb);
                 }
-                const uint32_t buf = kiter & 1, tph = (kiter >> 1) & 1;
-                if (!mbar_wait(tfull + buf, tph, abort_flag, prm.status, prm.timeout_ns, SITE_EPI_TMEM_FULL)) {
+                uint32_t n;
+                const int buf = seq.next(ks, NKS, park, n);
+                if (!mbar_wait(tfull + buf, n & 1, abort_flag, prm.status, prm.timeout_ns, SITE_EPI_TMEM_FULL)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const float s = a_cur * b_cur;
                 const uint32_t taddr = lane_base + buf * BN;
-                // 64 columns per TMEM load: the buffer is free again after
-                // HALF/64 load round trips, before the last 64 promotions.
-                uint32_t r[64];
+                const bool parks = park && ks == NKS - 1;   // this buffer takes the tile's partial
+                // 16-column TMEM loads, two in flight: the next one is issued before the
+                // current one's promotions.  The buffer is free again once the last load
+                // has landed, before the last 16 promotions.
+                constexpr int NC = HALF / 16;
+                uint32_t ra[16], rb[16];
+                tmem_ld_x16(taddr, ra);
+                tmem_wait_ld(ra);
 #pragma unroll
-                for (int c = 0; c < HALF / 64; ++c) {
-                    tmem_ld_x64(taddr + c * 64, r);
-                    tmem_wait_ld(r);
-                    if (c == HALF / 64 - 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(tempty + buf);
+                for (int c = 0; c < NC; ++c) {
+                    uint32_t(&cur)[16] = (c & 1) ? rb : ra;
+                    uint32_t(&nxt)[16] = (c & 1) ? ra : rb;
+                    if (c + 1 < NC)
+                        tmem_ld_x16(taddr + (c + 1) * 16, nxt);
+#pragma unroll
+                    for (int j = 0; j < 16; j += 2)
+                        fma2(acc[c * 16 + j], acc[c * 16 + j + 1], s, cur[j], cur[j + 1]);
+                    if (c + 1 < NC) {
+                        tmem_wait_ld(nxt);
+                        if (c + 2 == NC && !parks) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0)
+                                mbar_arrive(tempty + buf);
+                        }
                     }
-#pragma unroll
-                    for (int j = 0; j < 64; j += 2)
-                        fma2(acc[c * 64 + j], acc[c * 64 + j + 1], s, r[j], r[j + 1]);
                 }
-                ++kiter;
+                if (parks) {
+                    // the tile's sums go back into the columns this warp has just read;
+                    // the store warps copy them out and release the buffer
+#pragma unroll
+                    for (int c = 0; c < HALF / 32; ++c)
+                        tmem_st_x32(taddr + c * 32, &acc[c * 32]);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(park_full);
+                }
             }
             if (!ok)
                 break;
+            if (park)
+                continue;   // the store warps write the partial and signal its band
             // -------- tile store
             const int rows_valid = max(0, min(32, tc.valid_rows - q * 32));
             if (prm.o.out_mode == OUT_BF16) {
@@ -275,11 +349,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
                     }
                     store_chunk<4>(staging, v, base + c * 64, (int64_t)g.N * 2, rows_valid);
                 }
-            } else if (prm.o.out_mode == OUT_PARTIAL_F32) {
-                float4 *tb = partial_tile_base(prm.o, g, tc, BN);
-#pragma unroll
-                for (int c = 0; c < NCH; ++c)
-                    store_partial_chunk<BN>(tb, q, h * NCH + c, &acc[c * 32]);
             } else {
                 char *base = tile_out_base(prm.o, g, tc, 4) + ((int64_t)q * 32 * g.N + h * HALF) * 4;
 #pragma unroll
@@ -294,11 +363,58 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
                     store_chunk<8>(staging, v, base + c * 128, (int64_t)g.N * 4, rows_valid);
                 }
             }
-            if (prm.o.out_mode == OUT_PARTIAL_F32)
-                signals.add(prm.o, tc.b);
         }
-        if (ok)
-            signals.flush(prm.o);
+        __syncwarp();
+        if (lane == 0)
+            atomicAdd(const_cast<int *>(epi_done), 1);
+    } else {
+        setmaxnreg_dec<kRegsLow>();
+        if (park) {
+            // ------------------------------------------------ store warps: warp 12 + q copies
+            // lane quarter q (32 rows x BN columns) of each parked tile to its blocked
+            // partial, hands the buffer back to the MMA warp and publishes the band
+            // (batched per run of same-band tiles; 4 warps x 2 = the 8 signals a tile owes)
+            const int q = warp & 3;
+            const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+            BufSeq seq;
+            BandSignals signals;
+            uint32_t parked = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
+                const TileCoord tc = decode_tile<BN>(t, g);
+                int buf = 0;
+                uint32_t n;
+                for (int ks = 0; ks < NKS; ++ks)
+                    buf = seq.next(ks, NKS, true, n);
+                if (!mbar_wait(park_full, parked & 1, abort_flag, prm.status, prm.timeout_ns, SITE_PARK_FULL)) {
+                    ok = false;
+                    break;
+                }
+                ++parked;
+                tc_fence_after();
+                float4 *tb = partial_tile_base(prm.o, g, tc, BN);
+                const uint32_t taddr = lane_base + buf * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_x32(taddr + c * 32, r);
+                    tmem_wait_ld(r);
+                    if (c == BN / 32 - 1) {
+                        // the whole park is read: the MMA may refill the buffer
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive(tempty + buf);
+                            mbar_arrive(tempty + buf);
+                        }
+                    }
+                    store_partial_chunk<BN>(tb, q, c, reinterpret_cast<const float *>(r));
+                }
+                signals.add(prm.o, tc.b, 2);
+            }
+            if (ok)
+                signals.flush(prm.o);
+        }
         __syncwarp();
         if (lane == 0)
             atomicAdd(const_cast<int *>(epi_done), 1);
@@ -346,6 +462,10 @@ cudaError_t launch_gemm_blockscale(const BsParams &p, int bn, int grid, cudaStre
 
 int gemm_blockscale_num_regs(int bn) { return bn == 256 ? regs_of<256>() : regs_of<128>(); }
 
-int gemm_threads() { return kThreads; }
+bool gemm_blockscale_split_ok(int bn)
+{
+    const int regs = gemm_blockscale_num_regs(bn);
+    return regs >= 0 && (int64_t)regs * kThreads >= kRegsNeeded;
+}
 
 }  // namespace gemmar

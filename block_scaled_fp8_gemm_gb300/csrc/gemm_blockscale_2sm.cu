@@ -525,7 +525,7 @@ BsPlan plan_blockscale(int P, int64_t M, int64_t N, int64_t K, int bands, int sl
     if (use_pair && N % 256 == 0) {
         const int regs2 = gemm_blockscale_2sm_num_regs();
         const int clusters = gemm_blockscale_2sm_max_clusters();
-        if (clusters > 0 && regs2 >= 0 && (int64_t)regs2 * gemm_threads() >= 56 * 128 + 224 * 256) {
+        if (clusters > 0 && regs2 >= 0 && (int64_t)regs2 * kThreads >= kRegsLow * 128 + kRegsHigh * 256) {
             pl.pair = 1;
             pl.bn = 256;
             pl.box_b_rows = 128;

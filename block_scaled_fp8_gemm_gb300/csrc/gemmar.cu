@@ -191,8 +191,7 @@ TileGrid make_grid(int P, int64_t M, int64_t N, int64_t K, int bands, int bn, in
 // setmaxnreg; that split needs the kernel to have been built for 168 per thread.
 bool register_split_ok(int bn)
 {
-    const int regs = gemm_blockscale_num_regs(bn);
-    return regs >= 0 && (int64_t)regs * gemm_threads() >= 56 * 128 + 224 * 256;
+    return gemm_blockscale_split_ok(bn);
 }
 
 int64_t mx_sfa_bytes(int P, int64_t M, int64_t K, int bands)

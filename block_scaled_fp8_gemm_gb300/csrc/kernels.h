@@ -87,7 +87,9 @@ cudaError_t launch_gemm_ptpc(const MxParams &p, int bn, int grid, cudaStream_t s
 int gemm_blockscale_num_regs(int bn);
 int gemm_mx_num_regs(int bn);
 int gemm_ptpc_num_regs(int bn);
-int gemm_threads();
+// The one-CTA blockscale kernel was built with registers enough for its warp-role split
+// (setmaxnreg would wait forever otherwise).
+bool gemm_blockscale_split_ok(int bn);
 
 // Blockscale launch plan: CTA pairs (gemm_blockscale_2sm.cu, 256 x 128 pair
 // tiles) when the device can co-schedule two-CTA clusters, else one CTA per

@@ -130,8 +130,7 @@ extern "C" __attribute__((visibility("default"))) int fused_gemm_reduce_noalloc(
         return rc;
     const BsPlan pl = plan_blockscale(P, M, N, K, bands, 0, s->num_sms);
     if (!pl.pair) {
-        const int regs = gemm_blockscale_num_regs(pl.bn);
-        if (regs < 0 || (int64_t)regs * gemm_threads() < 56 * 128 + 224 * 256)
+        if (!gemm_blockscale_split_ok(pl.bn))
             return GEMMAR_ERR_DEVICE;
     }
     const int bn = pl.bn;
