@@ -251,7 +251,21 @@ __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGr
     const int64_t tile_f4 = 128 * (int64_t)bn / 4;
     const int64_t slice_f4 = tiles_per_band * tile_f4;
     const float4 *W = reinterpret_cast<const float4 *>(o.out);
-    int blk_even = -1, blk_odd = -1;   // block of items 8j..8j+7: blk_even for even j, blk_odd for odd
+    // block of items 8j..8j+7 (slot j & 1), decomposed once per claim: the lane's
+    // first source float4 of slice 0 and its row's first output column (null past
+    // the band end)
+    const float4 *src0 = nullptr, *src1 = nullptr;
+    uint16_t *out0 = nullptr, *out1 = nullptr;
+    auto decompose = [&](int blk, const float4 *&src, uint16_t *&out) {
+        const uint32_t b = (uint32_t)blk / bpb, r = (uint32_t)blk % bpb;
+        const int c = (int)(r % nchunk), q = (int)((r / nchunk) & 3);
+        const int64_t i = r / (4 * nchunk);
+        src = W + ((int64_t)b * P * tiles_per_band + i) * tile_f4 + ((q * nchunk + c) * 8) * 32 + lane;
+        const int mt = (int)(i / g.ntiles_n), nt = (int)(i % g.ntiles_n);
+        const int row = mt * 128 + q * 32 + lane;
+        out = row < g.rows_per_band ? o.red_out + ((int64_t)b * g.rows_per_band + row) * g.N + (int64_t)nt * bn + c * 32
+                                    : nullptr;
+    };
     // bf16 sums of the last four items: 16 columns of the lane's row
     uint32_t o0 = 0, o1 = 0, o2 = 0, o3 = 0, o4 = 0, o5 = 0, o6 = 0, o7 = 0;
     const bool out32 = (reinterpret_cast<uintptr_t>(o.red_out) & 31) == 0;
@@ -263,19 +277,16 @@ __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGr
         const int j = (k / IPB) & 1;
         if (more && k % IPB == 0) {
             const int claimed = claim_retired_block(o, g, bpb, cl, epi_done, epi_warps, timeout_ns);
-            if (j)
-                blk_odd = claimed;
-            else
-                blk_even = claimed;
             more = claimed >= 0;
+            if (more) {
+                if (j)
+                    decompose(claimed, src1, out1);
+                else
+                    decompose(claimed, src0, out0);
+            }
         }
         if (more) {
-            const uint32_t blk = (uint32_t)(j ? blk_odd : blk_even);
-            const uint32_t b = blk / bpb, r = blk % bpb;
-            const int c = (int)(r % nchunk), q = (int)((r / nchunk) & 3);
-            const int64_t i = r / (4 * nchunk);
-            const float4 *src = W + ((int64_t)b * P * tiles_per_band + i) * tile_f4 +
-                                ((q * nchunk + c) * 8 + k % IPB) * 32 + lane;
+            const float4 *src = (j ? src1 : src0) + (k % IPB) * 32;
             const uint32_t dst = ring + (k % RS) * STAGE + lane * 16;
             for (int p = 0; p < P; ++p)
                 ptx::cp_async_cg16(dst + p * 512, src + p * slice_f4);
@@ -297,11 +308,7 @@ __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGr
             a[0] = a[0] + __uint_as_float(v.x); a[1] = a[1] + __uint_as_float(v.y);
             a[2] = a[2] + __uint_as_float(v.z); a[3] = a[3] + __uint_as_float(v.w);
         }
-        const uint32_t blk = (uint32_t)(((k / IPB) & 1) ? blk_odd : blk_even);
-        const uint32_t b = blk / bpb, r = blk % bpb;
-        const int c = (int)(r % nchunk), q = (int)((r / nchunk) & 3);
-        const int64_t i = r / (4 * nchunk);
-        const int mt = (int)(i / g.ntiles_n), nt = (int)(i % g.ntiles_n);
+        uint16_t *const out = ((k / IPB) & 1) ? out1 : out0;
         // four consecutive items are 16 consecutive columns of the lane's row: 32
         // bytes, stored as one full sector once the fourth is summed
         {
@@ -312,11 +319,8 @@ __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGr
             o4 = slot == 2 ? lo : o4; o5 = slot == 2 ? hi : o5;
             o6 = slot == 3 ? lo : o6; o7 = slot == 3 ? hi : o7;
         }
-        const int row = mt * 128 + q * 32 + lane;   // row within the band
-        if ((k & 3) == 3 && row < g.rows_per_band) {
-            const int64_t m = (int64_t)b * g.rows_per_band + row;
-            const int64_t col = (int64_t)nt * bn + c * 32 + ((k % IPB) & 4) * 4;
-            uint16_t *dst = o.red_out + m * g.N + col;
+        if ((k & 3) == 3 && out != nullptr) {
+            uint16_t *dst = out + ((k % IPB) & 4) * 4;
             if (out32)   // rows are 32-byte multiples; the output base decides
                 asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(o0),
                              "r"(o1), "r"(o2), "r"(o3), "r"(o4), "r"(o5), "r"(o6), "r"(o7)

@@ -58,9 +58,10 @@ struct BsCfg {
 };
 
 constexpr int kThreads = 512;
-constexpr int kRegsLow = 56;    // warpgroups 0 (producer, MMA, reducers) and 3 (store warps) after setmaxnreg.dec
+constexpr int kRegsLow = 64;    // warpgroup 0 (producer, MMA, band reducers) after setmaxnreg.dec
+constexpr int kRegsStore = 48;  // warpgroup 3 (store warps) after setmaxnreg.dec
 constexpr int kRegsHigh = 200;  // warpgroups 1-2 (epilogue) after setmaxnreg.inc
-constexpr int kRegsNeeded = 2 * 128 * kRegsLow + 256 * kRegsHigh;
+constexpr int kRegsNeeded = 128 * kRegsLow + 128 * kRegsStore + 256 * kRegsHigh;
 static_assert(kRegsNeeded <= 65536, "register split");
 constexpr int kStoreWarps = 4;
 // K-blocks at the start of a band-path tile that run in one TMEM buffer while
@@ -368,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
         if (lane == 0)
             atomicAdd(const_cast<int *>(epi_done), 1);
     } else {
-        setmaxnreg_dec<kRegsLow>();
+        setmaxnreg_dec<kRegsStore>();
         if (park) {
             // ------------------------------------------------ store warps: warp 12 + q copies
             // lane quarter q (32 rows x BN columns) of each parked tile to its blocked
@@ -396,9 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_blockscale_kernel(const __gr
                 const uint32_t taddr = lane_base + buf * BN;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_x32(taddr + c * 32, r);
-                    tmem_wait_ld(r);
+                    uint32_t r[32], (&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[0]),
+                                    (&hi)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[16]);
+                    tmem_ld_x16(taddr + c * 32, lo);
+                    tmem_ld_x16(taddr + c * 32 + 16, hi);
+                    tmem_wait_ld(lo);
+                    tmem_wait_ld(hi);
                     if (c == BN / 32 - 1) {
                         // the whole park is read: the MMA may refill the buffer
                         tc_fence_before();

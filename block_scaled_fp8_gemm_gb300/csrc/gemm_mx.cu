@@ -63,8 +63,8 @@ constexpr int kThreads = 384;
 // Band path: pause between a warp's partial-store chunks (4 KB per warp), so a
 // tile's partial leaves over the next tile's compute rather than in one burst.
 constexpr unsigned kStorePaceNs = 600;
-constexpr int kRegsLow = 56;    // warpgroup 0 (producer, MMA) after setmaxnreg.dec
-constexpr int kRegsHigh = 224;  // warpgroups 1-2 (epilogue) after setmaxnreg.inc
+constexpr int kRegsLow = 64;    // warpgroup 0 (producer, MMA, band reducers) after setmaxnreg.dec
+constexpr int kRegsHigh = 216;  // warpgroups 1-2 (epilogue) after setmaxnreg.inc
 
 // Four channel scales.  The load is ordered after the preceding TMEM wait (asm
 // volatile) so the compiler keeps it next to its use instead of hoisting every
@@ -562,6 +562,8 @@ cudaError_t launch_gemm_ptpc(const MxParams &p, int bn, int grid, cudaStream_t s
 }
 
 int gemm_mx_num_regs(int bn) { return bn == 224 ? regs_of<224, false>() : regs_of<128, false>(); }
+
+bool gemm_mx_split_ok(int regs) { return regs >= 0 && (int64_t)regs * kThreads >= 128 * kRegsLow + 256 * kRegsHigh; }
 
 int gemm_ptpc_num_regs(int bn) { return bn == 256 ? regs_of<256, true>() : regs_of<128, true>(); }
 

@@ -188,7 +188,8 @@ TileGrid make_grid(int P, int64_t M, int64_t N, int64_t K, int bands, int bn, in
 }
 
 // The blockscale kernel splits 65536 registers between its warp roles with
-// setmaxnreg; that split needs the kernel to have been built for 168 per thread.
+// setmaxnreg; that split needs the kernel to have been built for 128 per thread
+// (512 threads).
 bool register_split_ok(int bn)
 {
     return gemm_blockscale_split_ok(bn);
@@ -242,7 +243,7 @@ int run_gemm(gemmar_ctx *ctx, int P, const uint8_t *const *A, const void *const 
         const int bn = ptpc_tile_n(N);
         if (slice_loop)
             bands = 1;
-        if (gemm_ptpc_num_regs(bn) * 384 < 56 * 128 + 224 * 256)
+        if (!gemm_mx_split_ok(gemm_ptpc_num_regs(bn)))
             return GEMMAR_ERR_DEVICE;
         MxParams prm;
         std::memset(&prm, 0, sizeof(prm));
@@ -262,7 +263,7 @@ int run_gemm(gemmar_ctx *ctx, int P, const uint8_t *const *A, const void *const 
         const int bn = mx_tile_n(N);
         if (slice_loop)
             bands = 1;
-        if (gemm_mx_num_regs(bn) * 384 < 56 * 128 + 224 * 256)
+        if (!gemm_mx_split_ok(gemm_mx_num_regs(bn)))
             return GEMMAR_ERR_DEVICE;
         if (mx_sfa_bytes(P, M, K, bands) > ctx->sfa_bytes || mx_sfb_bytes(P, N, K, bn) > ctx->sfb_bytes)
             return GEMMAR_ERR_WORKSPACE;

@@ -87,6 +87,9 @@ cudaError_t launch_gemm_ptpc(const MxParams &p, int bn, int grid, cudaStream_t s
 int gemm_blockscale_num_regs(int bn);
 int gemm_mx_num_regs(int bn);
 int gemm_ptpc_num_regs(int bn);
+// A whole-K kernel (mx or ptpc) built with `regs` per thread has registers enough for its
+// warp-role split.
+bool gemm_mx_split_ok(int regs);
 // The one-CTA blockscale kernel was built with registers enough for its warp-role split
 // (setmaxnreg would wait forever otherwise).
 bool gemm_blockscale_split_ok(int bn);
