@@ -86,8 +86,8 @@ enum { GEMMAR_SCALE_BLOCK128 = 0, GEMMAR_SCALE_MX32 = 1, GEMMAR_SCALE_PTPC = 2 }
                                              kernel (256 x 256 tiles over two SMs; band partials parked in
                                              shared memory and copied out by two store warps) instead of
                                              the one-CTA kernel; the same bits (tests); on the wo_b band
-                                             path its GEMM runs ~1810 us against ~1770 for the one-CTA
-                                             kernel, without the in-kernel band reduce */
+                                             path its GEMM runs ~1810 us against ~1680 for the one-CTA
+                                             kernel (both with the band reduce after the GEMM) */
 #define GEMMAR_FUSE_SLICES     (1u << 4)  /* fused: each output tile accumulates all P slices itself (no
                                              partials, no band reduce); see fused_gemm_reduce */
 #define GEMMAR_FUSE_ONCHIP     (1u << 6)  /* fused: the P slice partials of a tile stay on chip and are
@@ -280,10 +280,10 @@ int quant_mx_e4m3(gemmar_ctx *ctx, const void *x, int x_dtype, int64_t R, int64_
 /*
  * fused_gemm_reduce -- the whole wo_b path for P K-slices resident on this
  * GPU: one persistent GEMM launch over every (band, slice, tile) in band
- * order whose epilogue stores each tile's fp32 partial into the context's
- * workspace W[band][p] and signals that band's counter as soon as the tile
- * retires (sglang pull request #40757, "What": the fused kernel hands each
- * row band over as soon as that band's tiles are done).  Two spare warps of
+ * order that stores each tile's fp32 partial into the context's workspace
+ * W[band][p] and signals that band's counter as soon as the tile retires
+ * (sglang pull request #40757, "What": the fused kernel hands each row band
+ * over as soon as that band's tiles are done).  Two reducer warps of
  * every GEMM CTA take 32 x 32 output blocks of the bands already complete and
  * sum them while the GEMM still runs (the hand-over overlapped with the
  * compute, as the pages overlap their scatter with it; not on the CTA-pair
