@@ -464,6 +464,16 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[64])
 
 // Two independent fp32 fused multiply-adds (round to nearest, no flush):
 // (d.x, d.y) = (a * b.x + c.x, a * b.y + c.y) -- each lane exactly fmaf().
+// (x * a, y * b), each product rounded to nearest fp32 (one packed instruction)
+__device__ __forceinline__ float2 mul2(float x, float y, float a, float b)
+{
+    const uint64_t u = ((uint64_t)__float_as_uint(y) << 32) | __float_as_uint(x);
+    const uint64_t v = ((uint64_t)__float_as_uint(b) << 32) | __float_as_uint(a);
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(u), "l"(v));
+    return make_float2(__uint_as_float((uint32_t)d), __uint_as_float((uint32_t)(d >> 32)));
+}
+
 __device__ __forceinline__ void fma2(float &cx, float &cy, float a, uint32_t bx, uint32_t by)
 {
     uint64_t c = ((uint64_t)__float_as_uint(cy) << 32) | __float_as_uint(cx);

@@ -233,9 +233,12 @@ __device__ __forceinline__ uint32_t enc4(float a, float b, float c, float d, flo
 // included.  Otherwise (within ~2^-21 of a rounding midpoint) divide exactly.
 __device__ __forceinline__ uint32_t enc2_guarded(float a, float b, float s, float y)
 {
-    const float qa = __fmul_rn(a, y), qb = __fmul_rn(b, y);
-    const uint32_t lo = e4m3x2_from_f32(__fmul_rn(qa, 1.0f - 0x1p-21f), __fmul_rn(qb, 1.0f - 0x1p-21f));
-    const uint32_t hi = e4m3x2_from_f32(__fmul_rn(qa, 1.0f + 0x1p-21f), __fmul_rn(qb, 1.0f + 0x1p-21f));
+    // the same IEEE products, two per packed instruction
+    const float2 q = mul2(a, b, y, y);
+    const float2 l = mul2(q.x, q.y, 1.0f - 0x1p-21f, 1.0f - 0x1p-21f);
+    const float2 h = mul2(q.x, q.y, 1.0f + 0x1p-21f, 1.0f + 0x1p-21f);
+    const uint32_t lo = e4m3x2_from_f32(l.x, l.y);
+    const uint32_t hi = e4m3x2_from_f32(h.x, h.y);
     if (lo == hi)
         return lo;
     return e4m3x2_from_f32(__fdiv_rn(a, s), __fdiv_rn(b, s));
