@@ -201,27 +201,29 @@ def ctx_wide(g):
     c.close()
 
 
-@pytest.mark.parametrize("K", [128, 256, 384])
-def test_band_path_short_k_several_tiles_per_cta(g, ctx_wide, K):
-    """One, two and three K-blocks per tile with about three tiles per CTA (512
-    tiles on at most 152 CTAs).  The one-CTA kernel parks each tile's sums in the
-    TMEM buffer of its last K-block for the store warps; with fewer K-blocks than
-    its usual single-buffered lead the hand-over takes its capped form.  Against
-    the oracle, bit-equal to the same call with the reduce after the GEMM, and
-    twice the same bits."""
-    P, M, N, bands = 8, 1024, 2048, 4
-    A, sa, B, sb = blockscale_operands(P, M, N, K, seed=K + 17)
+@pytest.mark.parametrize("N,K", [(2048, 128), (2048, 256), (2048, 384), (1920, 128), (1920, 256)])
+def test_band_path_short_k_several_tiles_per_cta(g, ctx_wide, N, K):
+    """One, two and three K-blocks per tile with three or more tiles per CTA (512
+    tiles of 256 columns, or 960 of 128 columns when N is not a multiple of 256,
+    on at most 152 CTAs).  The one-CTA kernel parks each tile's sums in the TMEM
+    buffer of its last K-block for the store warps; with fewer K-blocks than its
+    usual single-buffered lead the hand-over takes its capped form.  Against the
+    oracle, bit-equal to the same call with the reduce after the GEMM, and twice
+    the same bits."""
+    P, M, bands = 8, 1024, 4
+    A, sa, B, sb = blockscale_operands(P, M, N, K, seed=K + N + 17)
     kind = g.GEMMAR_SCALE_BLOCK128
     band = run_fused(g, ctx_wide, A, sa, B, sb, kind, bands, flags=g.GEMMAR_DEBUG_CANARY)
     ov, tot = g.gemmar_overlap_stats(ctx_wide)
-    assert tot == bands * 2 * (N // 256) * 4 * 8 and 0 <= ov <= tot
+    bn = 256 if N % 256 == 0 else 128
+    assert tot == bands * 2 * (N // bn) * 4 * (bn // 32) and 0 <= ov <= tot
     again = run_fused(g, ctx_wide, A, sa, B, sb, kind, bands)
     serial = run_fused(g, ctx_wide, A, sa, B, sb, kind, bands,
                        flags=g.GEMMAR_SERIAL_REDUCE | g.GEMMAR_DEBUG_CANARY)
     assert torch.equal(band.view(torch.int16), again.view(torch.int16))
     assert torch.equal(band.view(torch.int16), serial.view(torch.int16))
     ref, _ = oracle.gemm_reduce(A, sa, B, sb, 0)
-    check_bf16_output(band.float().cpu().numpy(), ref, f"band path K={K} (3 tiles per CTA)")
+    check_bf16_output(band.float().cpu().numpy(), ref, f"band path N={N} K={K} (3 or more tiles per CTA)")
 
 
 def test_fused_fp8_wire(g, ctx):
