@@ -335,6 +335,94 @@ __device__ __forceinline__ void band_reducer_warp(const GemmOut &o, const TileGr
     ptx::cp_async_wait<0>();
 }
 
+// Band-reduce work for warps with time and registers to spare between tiles
+// (the whole-K kernel's epilogue warps, whose next tile computes in the other
+// TMEM buffer): a warp holds one claimed 32 x 32 block at a time and sums one
+// item of it per step -- one 16-byte column unit of each lane's row over all P
+// slices, in the band reducer's order ((W_0 + W_1) + ...) in fp32 then bf16 --
+// with plain loads into registers.  Claims never wait: a band that is not
+// complete yet is tried again at the next call.  A block once claimed is
+// finished (finish()) before the warp counts itself out, as band_reduce then
+// skips it.
+struct SpareReducer {
+    const float4 *src = nullptr;   // the lane's 16 bytes of item 0, slice 0, of the held block
+    uint16_t *out = nullptr;       // the lane's row, first column of the block (null past the band end)
+    int item = 8;                  // next item of the held block; 8: none held
+    int band = 0;                  // lowest band that may still have unclaimed blocks (lane 0)
+    int ready_upto = -1;           // bands <= ready_upto have been seen complete (lane 0)
+
+    // take a block if none is held and one is free; false if none is held afterwards.
+    // Whole warp calls.
+    __device__ __forceinline__ bool hold(const GemmOut &o, const TileGrid &g, int bn)
+    {
+        if (item < 8)
+            return true;
+        const int nchunk = bn / 32;
+        const int64_t tiles_per_band = (int64_t)g.mt_per_band * g.ntiles_n;
+        const uint32_t bpb = (uint32_t)(tiles_per_band * 4 * nchunk);
+        int blk = -1;
+        if ((threadIdx.x & 31) == 0) {
+            while (band < g.bands) {
+                if (band > ready_upto) {
+                    if (ptx::ld_acquire(o.band_done + band) < o.band_expected)
+                        break;   // not complete yet: the next call tries again
+                    ready_upto = band;
+                }
+                const uint32_t r = atomicAdd(o.reduce_next + band, 1u);
+                if (r < bpb) {
+                    blk = (int)((uint32_t)band * bpb + r);
+                    break;
+                }
+                ++band;
+            }
+        }
+        blk = __shfl_sync(0xffffffffu, blk, 0);
+        if (blk < 0)
+            return false;
+        const int lane = threadIdx.x & 31;
+        const uint32_t b = (uint32_t)blk / bpb, r = (uint32_t)blk % bpb;
+        const int c = (int)(r % nchunk), q = (int)((r / nchunk) & 3);
+        const int64_t i = r / (4 * nchunk);
+        const int64_t tile_f4 = 128 * (int64_t)bn / 4;
+        src = reinterpret_cast<const float4 *>(o.out) + ((int64_t)b * g.P * tiles_per_band + i) * tile_f4 +
+              ((q * nchunk + c) * 8) * 32 + lane;
+        const int mt = (int)(i / g.ntiles_n), nt = (int)(i % g.ntiles_n);
+        const int row = mt * 128 + q * 32 + lane;
+        out = row < g.rows_per_band ? o.red_out + ((int64_t)b * g.rows_per_band + row) * g.N + (int64_t)nt * bn + c * 32
+                                    : nullptr;
+        item = 0;
+        return true;
+    }
+
+    // sum and store the next item of the held block.  Whole warp calls.
+    __device__ __forceinline__ void step(const GemmOut &o, const TileGrid &g, int bn)
+    {
+        const int64_t slice_f4 = (int64_t)g.mt_per_band * g.ntiles_n * (128 * (int64_t)bn / 4);
+        const float4 *s = src + item * 32;
+        float4 v[kMaxP];
+#pragma unroll
+        for (int p = 0; p < kMaxP; ++p)
+            if (p < g.P)
+                v[p] = __ldcs(s + p * slice_f4);
+        float a0 = v[0].x, a1 = v[0].y, a2 = v[0].z, a3 = v[0].w;
+#pragma unroll
+        for (int p = 1; p < kMaxP; ++p)
+            if (p < g.P) {
+                a0 = a0 + v[p].x; a1 = a1 + v[p].y; a2 = a2 + v[p].z; a3 = a3 + v[p].w;
+            }
+        if (out != nullptr)
+            *reinterpret_cast<uint2 *>(out + item * 4) = make_uint2(ptx::bf16x2_from_f32(a0, a1), ptx::bf16x2_from_f32(a2, a3));
+        ++item;
+    }
+
+    // sum what is left of the held block.  Whole warp calls.
+    __device__ __forceinline__ void finish(const GemmOut &o, const TileGrid &g, int bn)
+    {
+        while (item < 8)
+            step(o, g, bn);
+    }
+};
+
 template <int N>
 __device__ __forceinline__ void setmaxnreg_dec()
 {

@@ -409,6 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                 }
             }
         }
+        // band path with the in-kernel reduce: between tiles the epilogue warps sum
+        // band-reduce items too (their next tile computes in the other TMEM buffer)
+        const bool assist = !exact && prm.o.out_mode == OUT_PARTIAL_F32 && prm.o.reduce_next != nullptr;
+        SpareReducer spare;
         for (int t = blockIdx.x; t < g.num_tiles && !exact; t += gridDim.x) {
             const TileCoord tc = decode_tile<BN>(t, g);
             const float sa_m = PT ? __ldg(prm.pa[tc.p] + min(tc.m0 + q * 32 + lane, g.M - 1)) : 0.0f;
@@ -466,6 +470,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
                 }
                 signals.add(prm.o, tc.b);
                 ++titer;
+                if (assist && t + (int)gridDim.x < g.num_tiles) {
+                    // until the next tile's accumulator is complete (the MMA needs this
+                    // buffer back only for the tile after next); not after the last tile,
+                    // whose band signals the flush below still has to publish
+                    while (!mbar_test_wait(tfull + (titer & 1), (titer >> 1) & 1) && spare.hold(prm.o, g, BN))
+                        spare.step(prm.o, g, BN);
+                }
                 continue;
             }
             for (int c = h; c < NCH; c += 2) {
@@ -508,6 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_mx_kernel(const __grid_const
         }
         if (!exact)
             signals.flush(prm.o);
+        if (assist)
+            spare.finish(prm.o, g, BN);   // band_reduce skips a claimed block
         __syncwarp();
         if (lane == 0)
             atomicAdd(const_cast<int *>(epi_done), 1);
