@@ -4,7 +4,7 @@
 // scale_vec::1X, the scales read from TMEM, accumulation over the whole K in
 // TMEM -- no promotion on the CUDA cores.
 //
-// Same persistent, warp-specialised layout as the blockscale kernel:
+// Persistent and warp-specialised, one CTA of 12 warps per SM:
 //   warp 0     TMA producer: A 128x128, B BNx128 tiles (128-byte swizzle) and
 //              the stage's repacked scale images (512 + 1024 bytes, bulk copy).
 //   warp 1     MMA issuer: per stage, tcgen05.cp of the scale images into
@@ -13,8 +13,11 @@
 //              byte of the 32-bit scale word).  tcgen05.cp and tcgen05.mma
 //              issued by one thread execute in order, so one TMEM scale slot
 //              serves every stage.
+//   warps 2-3  band path: band reducers (epilogue.cuh).
 //   warps 4-11 epilogue: drain the tile's fp32 accumulator (double-buffered
-//              across tiles) in 32-column chunks and store it.
+//              across tiles) in 32-column chunks and store it.  On the band
+//              path with the in-kernel reduce they also sum band-reduce items
+//              between tiles, until the next tile's accumulator is complete.
 // With the slice partials summed on chip (TileGrid::slice_loop == 2) every
 // slice of a tile accumulates from zero in its own TMEM buffer -- exactly the
 // band path's partial -- and the epilogue folds it into a register running sum
