@@ -454,6 +454,27 @@ def run_ours(args, rank, world, local_rank):
         "note": "GEMMAR_SERIAL_REDUCE: the GEMM reduces nothing while it runs; band_reduce sums every "
                 "block after it (same output bits)"}
 
+    # ---- the GEMM alone (gemm_blockscale_fp8), one slice to bf16: the pages' GEMM-only
+    # configuration.  Steps rotate over the 8 slices' operands (376 MB, more than L2).
+    c1 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    g1_next = [0]
+
+    def step_g1():
+        p = g1_next[0] % P
+        g1_next[0] += 1
+        g.gemm_blockscale_fp8(ctx, A[p], sa[p], B[p], sb[p], c1)
+
+    for _ in range(P):
+        step_g1()
+    ms_g1 = time_steps(step_g1, max(8, args.steps // 2), stream)
+    fl1 = 2.0 * M * N * K
+    extra["gemm_only"] = {
+        "us": ms_g1 * 1e3, "tflops": fl1 / (ms_g1 * 1e-3) / 1e12,
+        "frac_of_fp8_peak": fl1 / (ms_g1 * 1e-3) / 1e12 / fp8_peak,
+        "what": "gemm_blockscale_fp8 on one slice, [16384, 2048] x [7168, 2048]^T with 1x128 / 128x128 fp32 "
+                "scales to bf16; the pages quote 369.4 us for this GEMM on one MI355X (context, not a target)"}
+    del c1
+
     # ---- the band_reduce entry point on its own: row-major fp32 partials
     # [bands][P][M/bands][N] of the headline size, summed to bf16
     W_rm = torch.randn((P, M, N), dtype=torch.float32, device=dev)
