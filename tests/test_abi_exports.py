@@ -64,6 +64,10 @@ def test_shape_rules_host_only(lib):
     assert sup(9, 128, 256, 128, 1, 0) == ARG           # more slices than the ABI takes
     assert sup(2, 128, 256, 128, 0, 0) == ARG
     assert sup(2, 128, 256, 128, 2, 7) == ARG           # unknown scale kind
+    # empty inputs: zero rows, columns, K or slices are argument errors (nothing to launch)
+    for empty in [(8, 0, 7168, 2048, 8, 0), (4, 0, 7168, 2048, 4, 1), (1, 128, 0, 2048, 1, 0),
+                  (1, 128, 7168, 0, 1, 0), (0, 128, 256, 128, 1, 0)]:
+        assert sup(*empty) == ARG, empty
 
 
 def declared_constants():

@@ -55,6 +55,31 @@ def test_host_side_errors_launch_nothing(g):
     ctx.close()
 
 
+def test_empty_inputs_are_refused_before_any_launch(g):
+    """Zero rows through every entry point: refused on the host (argument or shape
+    error), nothing launched, the context's status clean afterwards."""
+    torch.cuda.set_device(0)
+    ctx = g.gemmar_create(0, 256, 512, 256, 2, flags=g.GEMMAR_NO_SELF_TEST)
+    u8 = lambda *s: torch.empty(s, dtype=torch.uint8, device="cuda")
+    f32 = lambda *s: torch.empty(s, dtype=torch.float32, device="cuda")
+    bf = lambda *s: torch.empty(s, dtype=torch.bfloat16, device="cuda")
+    B, sb = [u8(512, 256)] * 2, [f32(4, 2)] * 2
+    calls = {
+        "fused_gemm_reduce": lambda: g.fused_gemm_reduce(ctx, [u8(0, 256)] * 2, [f32(0, 2)] * 2, B, sb, bf(0, 512)),
+        "gemm_blockscale_fp8": lambda: g.gemm_blockscale_fp8(ctx, u8(0, 256), f32(0, 2), B[0], sb[0], bf(0, 512)),
+        "rowquant_e4m3": lambda: g.rowquant_e4m3(ctx, bf(0, 512), u8(0, 512), f32(0)),
+        "rowdequant_e4m3": lambda: g.rowdequant_e4m3(ctx, u8(0, 512), f32(0), bf(0, 512)),
+        "quant_blockscale_e4m3": lambda: g.quant_blockscale_e4m3(ctx, bf(0, 256), 1, u8(0, 256), f32(0, 2)),
+    }
+    for name, call in calls.items():
+        with pytest.raises(g.GemmarError) as e:
+            call()
+        assert e.value.code in (g.GEMMAR_ERR_ARG, g.GEMMAR_ERR_SHAPE), (name, e.value.code)
+    torch.cuda.synchronize()
+    assert g.gemmar_status(ctx) == (0, 0)
+    ctx.close()
+
+
 @pytest.mark.parametrize("kind,create_flags,call_flags",
                          [(0, 0, 0), (0, "pair", 0), (1, 0, 0), (2, 0, 0), (0, 0, "fuse_quantize")],
                          ids=["blockscale", "blockscale-cta-pair", "mx", "ptpc", "blockscale-fused-quantize"])
