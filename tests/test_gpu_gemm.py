@@ -248,6 +248,23 @@ def test_fused_fp8_wire(g, ctx):
     assert torch.equal(y.view(torch.int16), wire.view(torch.int16))
 
 
+@pytest.mark.parametrize("N", [12288, 12544])
+def test_fused_quantize_at_its_width_limit(g, N):
+    """The folded quantiser parks 8 bf16 rows of N in shared memory, N <= 12288
+    (192 KB at the limit); above it the flag is ignored.  Either way the output
+    is the unfolded wire's, bit for bit."""
+    P, M, K, bands = 2, 256, 256, 2
+    c = g.gemmar_create(0, M, N, K, P, flags=g.GEMMAR_NO_SELF_TEST, wait_timeout_ns=1_000_000_000)
+    try:
+        A, sa, B, sb = blockscale_operands(P, M, N, K, seed=N)
+        kind = g.GEMMAR_SCALE_BLOCK128
+        wire = run_fused(g, c, A, sa, B, sb, kind, bands, flags=g.GEMMAR_FP8_WIRE)
+        fold = run_fused(g, c, A, sa, B, sb, kind, bands, flags=g.GEMMAR_FP8_WIRE | g.GEMMAR_FUSE_QUANTIZE)
+        assert torch.equal(wire.view(torch.int16), fold.view(torch.int16))
+    finally:
+        c.close()
+
+
 @pytest.mark.parametrize("serial", [False, True])
 @pytest.mark.parametrize("kind", [0, 1, 2])
 @pytest.mark.parametrize("P,M,N,K,bands", [(8, 1024, 1024, 512, 8), (3, 600, 896, 384, 3), (2, 256, 512, 256, 2)])
