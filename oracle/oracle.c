@@ -205,12 +205,16 @@ void orc_quant_block(const float *x, int64_t R, int64_t C, int64_t gr, int64_t g
  * plus one unless r is an exact power of two -- so it is exact at powers of
  * two, where a floating log2 can land one too high ([PR43480] item 7).
  * frexp gives the representation exactly, subnormals included.  Returns the
- * stored byte e + 127, clamped to [0, 254]; r == 0 gives byte 0 (R3).
+ * stored byte e + 127, clamped to [0, 254]; r == 0 gives byte 0 (R3).  An
+ * infinite r (a group holding an infinity) lies above every power of two and
+ * takes the upper clamp; frexp does not define an exponent for it.
  */
 uint8_t orc_ue8m0_byte(float r)
 {
     if (!(r > 0.0f))
         return 0;
+    if (isinf(r))
+        return 254;
     int e2;
     double fr = frexp((double)r, &e2);   /* r = fr * 2^e2, fr in [0.5, 1) */
     int e = (fr == 0.5) ? e2 - 1 : e2;   /* exact power of two: log2 r = e2-1 */

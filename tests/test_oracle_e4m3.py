@@ -185,3 +185,14 @@ def test_ue8m0_matches_exact_ceil_log2():
         e = ceil_log2_exact(Fraction(float(v)))
         assert oracle.ue8m0_byte(float(v)) == max(0, min(254, e + 127)), v
     assert oracle.ue8m0_byte(0.0) == 0
+
+
+def test_ue8m0_clamps_at_the_top_of_the_range():
+    # ceil(log2 r) grows without bound as r does and the byte is clamped to 254: the largest
+    # finite ratio (fp32 max / 448 ~ 2^119.2) still has its own exponent, and an infinite
+    # ratio (a group holding an infinity) takes the clamp like any ratio above 2^127
+    big = np.float32(np.finfo(np.float32).max / np.float32(448.0))
+    assert oracle.ue8m0_byte(float(big)) == ceil_log2_exact(Fraction(float(big))) + 127
+    assert oracle.ue8m0_byte(float(np.float32(2.0 ** 127))) == 254
+    assert oracle.ue8m0_byte(float(np.nextafter(np.float32(2.0 ** 127), np.float32(np.inf)))) == 254
+    assert oracle.ue8m0_byte(float("inf")) == 254
