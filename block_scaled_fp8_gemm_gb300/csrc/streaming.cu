@@ -542,11 +542,13 @@ struct Lane16 {
             v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         }
     }
+    // max |v| with NaN skipped (fmaxf returns the other operand), from 0: a lane of
+    // NaN alone gives 0, as a group of NaN alone must (scale 0, +0 codes)
     __device__ __forceinline__ float amax() const
     {
-        float m = fabsf(v[0]);
+        float m = 0.0f;
 #pragma unroll
-        for (int i = 1; i < V; ++i)
+        for (int i = 0; i < V; ++i)
             m = fmaxf(m, fabsf(v[i]));
         return m;
     }

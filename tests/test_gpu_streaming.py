@@ -94,6 +94,52 @@ def test_rowcodec_edge_cases(g, ctx):
         assert np.array_equal(y, oracle.rowdequant(q_ref, s_ref))
 
 
+def _nan_as_one(codes):
+    """e4m3 codes with both NaN codes (0x7F, 0xFF) mapped to 0x7F: the sign of a
+    NaN is not something the encoding fixes."""
+    c = np.asarray(codes, dtype=np.uint8).copy()
+    c[(c & 0x7F) == 0x7F] = 0x7F
+    return c
+
+
+def _non_finite_rows(C):
+    x = synthetic.normal(5, synthetic.TID_X, 5, (6, C))
+    x[0, 7] = np.inf                                 # one +inf: scale inf, the rest +-0 codes, inf -> NaN
+    x[1, 9] = -np.inf
+    x[2, 11] = np.nan                                # a NaN is skipped by the amax, coded NaN
+    x[3] = np.nan                                    # all NaN: amax 0, scale 0, +0 codes
+    x[4, 3], x[4, C - 1] = np.inf, -np.inf
+    return x                                         # row 5: finite control
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_quantisers_with_non_finite_inputs(g, ctx, dtype):
+    """Infinities and NaN in the quantised rows (an overflowing layer): the row
+    codec's and the 1x128 and mx quantisers' codes and scales match the oracle,
+    the two NaN codes taken as one."""
+    C = 256
+    xd, xw = _as_input(_non_finite_rows(C), dtype)
+    q = torch.empty((6, C), dtype=torch.uint8, device="cuda")
+    s = torch.empty((6,), dtype=torch.float32, device="cuda")
+    g.rowquant_e4m3(ctx, xd, q, s)
+    sg = torch.empty((6, C // 128), dtype=torch.float32, device="cuda")
+    qg = torch.empty((6, C), dtype=torch.uint8, device="cuda")
+    g.quant_blockscale_e4m3(ctx, xd, 1, qg, sg)
+    em = torch.empty((6, C // 32), dtype=torch.uint8, device="cuda")
+    qm = torch.empty((6, C), dtype=torch.uint8, device="cuda")
+    g.quant_mx_e4m3(ctx, xd, qm, em)
+    assert_status_ok(g, ctx)
+    q_ref, s_ref = oracle.rowquant(xw)
+    assert np.array_equal(s.cpu().numpy(), s_ref)
+    assert np.array_equal(_nan_as_one(q.cpu().numpy()), _nan_as_one(q_ref))
+    qg_ref, sg_ref = oracle.quant_block(xw, 1, 128)
+    assert np.array_equal(sg.cpu().numpy(), sg_ref)
+    assert np.array_equal(_nan_as_one(qg.cpu().numpy()), _nan_as_one(qg_ref))
+    qm_ref, em_ref = oracle.quant_mx(xw)
+    assert np.array_equal(em.cpu().numpy(), em_ref)
+    assert np.array_equal(_nan_as_one(qm.cpu().numpy()), _nan_as_one(qm_ref))
+
+
 def test_rowdequant_all_codes(g, ctx):
     codes = np.arange(256, dtype=np.uint8)
     codes[codes == 0x7F] = 0x7E
