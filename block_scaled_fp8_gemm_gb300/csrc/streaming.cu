@@ -225,18 +225,22 @@ __device__ __forceinline__ uint32_t enc4(float a, float b, float c, float d, flo
     return lo | (hi << 16);
 }
 
-// e4m3 codes of RN(a/s) and RN(b/s) without dividing, given y = RN(1/s)
-// (s > 0 and 1/s finite).  q = a*y is within 3*2^-24 relative of a/s, and so
-// of RN(a/s); the products q*(1 -+ 2^-21) -- rounded -- still enclose that
-// neighbourhood.  Rounding to e4m3 (nearest-even, saturating) is monotone, so
-// when both ends give the same code every value between them does, RN(a/s)
-// included.  Otherwise (within ~2^-21 of a rounding midpoint) divide exactly.
-__device__ __forceinline__ uint32_t enc2_guarded(float a, float b, float s, float y)
+// e4m3 codes of RN(a/s) and RN(b/s) without dividing, given yl = RN(y(1 - 2^-21))
+// and yh = RN(y(1 + 2^-21)) for y = RN(1/s) (s > 0, y a normal number).  The
+// products l = RN(a yl) and h = RN(a yh) are a/s times (1 -+ 2^-21) and three
+// rounding factors, each within 2^-24 of 1; (1 + 2^-24)^3 < 1 + 2^-21, so |l| <
+// |a/s| < |h| (below the normal range, all three round to a zero code anyway).
+// Rounding to e4m3 (nearest-even, saturating) is monotone, so when l and h give
+// the same code every value between them does, RN(a/s) included.  Otherwise a/s
+// lies within ~2^-21 of a code midpoint: divide exactly.  With bf16 inputs this
+// happens to ~0.5% of the values (x 448 / amax is then exactly a midpoint), so
+// the division stays per pair: a fallback for a whole lane's values would be
+// taken by most warps.
+__device__ __forceinline__ uint32_t enc2_guarded(float a, float b, float s, float yl, float yh)
 {
-    // the same IEEE products, two per packed instruction
-    const float2 q = mul2(a, b, y, y);
-    const float2 l = mul2(q.x, q.y, 1.0f - 0x1p-21f, 1.0f - 0x1p-21f);
-    const float2 h = mul2(q.x, q.y, 1.0f + 0x1p-21f, 1.0f + 0x1p-21f);
+    // the products two per packed instruction
+    const float2 l = mul2(a, b, yl, yl);
+    const float2 h = mul2(a, b, yh, yh);
     const uint32_t lo = e4m3x2_from_f32(l.x, l.y);
     const uint32_t hi = e4m3x2_from_f32(h.x, h.y);
     if (lo == hi)
@@ -244,23 +248,32 @@ __device__ __forceinline__ uint32_t enc2_guarded(float a, float b, float s, floa
     return e4m3x2_from_f32(__fdiv_rn(a, s), __fdiv_rn(b, s));
 }
 
-// Row/group encoder: the guarded multiply when 1/s is a finite normal number,
-// exact division otherwise (s == 0 gives +0 codes).
+// Row/group encoder: the guarded products when 1/s is a normal number below
+// 2^125, exact division otherwise (s == 0 gives +0 codes).  s = amax / 448 is at
+// most FLT_MAX / 448, so y is never subnormal; s = inf gives y = 0 and products
+// equal to the exact quotients' codes (+-0, and NaN for an infinite input).
 struct Enc {
-    float s, y;
+    float s, yl, yh;
     bool fast;
     __device__ __forceinline__ explicit Enc(float sc) : s(sc)
     {
-        y = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
-        fast = sc >= 0x1p-125f;   // 1/s < 2^125: finite, and q*(1+2^-21) cannot overflow
+        const float y = sc > 0.0f ? __frcp_rn(sc) : 0.0f;
+        yl = __fmul_rn(y, 1.0f - 0x1p-21f);
+        yh = __fmul_rn(y, 1.0f + 0x1p-21f);
+        fast = sc >= 0x1p-125f;   // 1/s <= 2^125: finite, and y (1 + 2^-21) cannot overflow
     }
     // from the fields of an encoder built earlier (kept in shared memory)
-    __device__ __forceinline__ Enc(float sc, float y_, bool fast_) : s(sc), y(y_), fast(fast_) {}
+    __device__ __forceinline__ Enc(float sc, float yl_, float yh_, bool fast_) : s(sc), yl(yl_), yh(yh_), fast(fast_) {}
     __device__ __forceinline__ uint32_t operator()(float a, float b, float c, float d) const
     {
         if (!fast)
             return enc4(a, b, c, d, s);
-        return enc2_guarded(a, b, s, y) | (enc2_guarded(c, d, s, y) << 16);
+        return enc2_guarded(a, b, s, yl, yh) | (enc2_guarded(c, d, s, yl, yh) << 16);
+    }
+    // the four codes of two packed bf16 pairs (low half first)
+    __device__ __forceinline__ uint32_t bf16x4(uint32_t w0, uint32_t w1) const
+    {
+        return (*this)(bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1));
     }
 };
 
@@ -381,7 +394,7 @@ __global__ void __launch_bounds__(kRqThreads, 2) band_reduce_quant_kernel(
     extern __shared__ __align__(16) uint8_t rq_smem[];
     uint16_t *park = reinterpret_cast<uint16_t *>(rq_smem);   // [kRqRows][N] bf16
     __shared__ float red[kRqThreads / 32][kRqRows];
-    __shared__ float enc_s[kRqRows], enc_y[kRqRows];
+    __shared__ float enc_s[kRqRows], enc_yl[kRqRows], enc_yh[kRqRows];
     __shared__ int enc_fast[kRqRows];
     __shared__ int band_ok;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -468,7 +481,8 @@ __global__ void __launch_bounds__(kRqThreads, 2) band_reduce_quant_kernel(
         const float sc = __fdiv_rn(a, 448.0f);
         const Enc e(sc);
         enc_s[t] = e.s;
-        enc_y[t] = e.y;
+        enc_yl[t] = e.yl;
+        enc_yh[t] = e.yh;
         enc_fast[t] = e.fast ? 1 : 0;
         if (row0 + t < rows_per_band)
             s[(int64_t)b * rows_per_band + row0 + t] = sc;
@@ -480,7 +494,7 @@ __global__ void __launch_bounds__(kRqThreads, 2) band_reduce_quant_kernel(
         const int rr = i / per_row, g = i - rr * per_row;
         if (row0 + rr >= rows_per_band)
             break;   // rows past the band end come last
-        const Enc e(enc_s[rr], enc_y[rr], enc_fast[rr] != 0);
+        const Enc e(enc_s[rr], enc_yl[rr], enc_yh[rr], enc_fast[rr] != 0);
         const uint4 w = *reinterpret_cast<const uint4 *>(park + rr * N + g * 8);
         uint2 o;
         o.x = e(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
@@ -582,46 +596,67 @@ __device__ __forceinline__ float segment_max(float m)
 // per-group scale arithmetic (an IEEE division and reciprocal, executed by
 // every lane of the group) is spread over 16 values per lane.  (Four lanes of
 // 32 values halve that share but need 93 registers, two CTAs per SM, and ran
-// slower.)  With C % 128 == 0 group gi = row * (C/128) + g starts at element
-// 128 * gi, so the groups are walked as one flat sequence.
+// slower; one division per two warp steps, lane j of a group dividing for step
+// j % 2, ran slower too.)  With C % 128 == 0 group gi = row * (C/128) + g
+// starts at element 128 * gi, so the groups are walked as one flat sequence.
 constexpr int kQSteps = 2;    // warp steps with loads in flight together
 constexpr int kQLanes = 8;    // lanes per group
 constexpr int kQVals = 128 / kQLanes;
 
+// A lane's 16 values as loaded: bf16 as 8 packed pairs, unpacked where they are
+// used (holding them unpacked cost registers and 12% of the kernel's time), or
+// 16 fp32 bit patterns.
 template <bool BF16>
 struct Lane16x {
-    static constexpr int NL = kQVals / Lane16<BF16>::V;   // 16-byte loads per lane
-    Lane16<BF16> part[NL];
+    static constexpr int NW = BF16 ? kQVals / 2 : kQVals;
+    uint32_t w[NW];
     __device__ __forceinline__ void load(const void *x, int64_t e)
     {
+        const uint4 *src = BF16 ? reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(x) + e)
+                                : reinterpret_cast<const uint4 *>(reinterpret_cast<const float *>(x) + e);
 #pragma unroll
-        for (int i = 0; i < NL; ++i)
-            part[i].load(x, e + i * Lane16<BF16>::V);
+        for (int i = 0; i < NW / 4; ++i) {
+            const uint4 v = __ldcs(src + i);
+            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        }
     }
+    // the k-th of the four-value quads, as fp32
+    __device__ __forceinline__ float4 quad(int k) const
+    {
+        if constexpr (BF16)
+            return make_float4(bf16_lo(w[2 * k]), bf16_hi(w[2 * k]), bf16_lo(w[2 * k + 1]), bf16_hi(w[2 * k + 1]));
+        else
+            return make_float4(__uint_as_float(w[4 * k]), __uint_as_float(w[4 * k + 1]), __uint_as_float(w[4 * k + 2]),
+                               __uint_as_float(w[4 * k + 3]));
+    }
+    // max |v| with NaN skipped, from 0 (a group of NaN alone gives 0)
     __device__ __forceinline__ float amax() const
     {
-        float m = part[0].amax();
+        float m = 0.0f;
 #pragma unroll
-        for (int i = 1; i < NL; ++i)
-            m = fmaxf(m, part[i].amax());
+        for (int k = 0; k < kQVals / 4; ++k) {
+            const float4 v = quad(k);
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
         return m;
     }
     __device__ __forceinline__ void store_codes(uint8_t *q, int64_t e, const Enc &enc) const
     {
-        uint32_t w[kQVals / 4];
+        uint32_t c[kQVals / 4];
+        if (enc.fast) {
 #pragma unroll
-        for (int i = 0; i < NL; ++i) {
-            const float *v = part[i].v;
-            if constexpr (BF16) {
-                w[2 * i] = enc(v[0], v[1], v[2], v[3]);
-                w[2 * i + 1] = enc(v[4], v[5], v[6], v[7]);
-            } else {
-                w[i] = enc(v[0], v[1], v[2], v[3]);
+            for (int k = 0; k < kQVals / 4; ++k) {
+                const float4 v = quad(k);
+                c[k] = enc2_guarded(v.x, v.y, enc.s, enc.yl, enc.yh) | (enc2_guarded(v.z, v.w, enc.s, enc.yl, enc.yh) << 16);
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < kQVals / 4; ++k) {
+                const float4 v = quad(k);
+                c[k] = enc4(v.x, v.y, v.z, v.w, enc.s);
             }
         }
-#pragma unroll
-        for (int i = 0; i < kQVals / 16; ++i)
-            *reinterpret_cast<uint4 *>(q + e + 16 * i) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        *reinterpret_cast<uint4 *>(q + e) = make_uint4(c[0], c[1], c[2], c[3]);
     }
 };
 

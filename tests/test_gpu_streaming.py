@@ -112,12 +112,13 @@ def _non_finite_rows(C):
     return x                                         # row 5: finite control
 
 
+@pytest.mark.parametrize("C", [256, 1024])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_quantisers_with_non_finite_inputs(g, ctx, dtype):
+def test_quantisers_with_non_finite_inputs(g, ctx, dtype, C):
     """Infinities and NaN in the quantised rows (an overflowing layer): the row
     codec's and the 1x128 and mx quantisers' codes and scales match the oracle,
-    the two NaN codes taken as one."""
-    C = 256
+    the two NaN codes taken as one.  bf16 rows of 1024 take the single-pass row
+    quantiser, whose amax runs on packed bf16 pairs."""
     xd, xw = _as_input(_non_finite_rows(C), dtype)
     q = torch.empty((6, C), dtype=torch.uint8, device="cuda")
     s = torch.empty((6,), dtype=torch.float32, device="cuda")
