@@ -132,3 +132,52 @@ def test_mx_quant_properties():
     assert np.all(np.abs(deq - x)[nz] <= bound[nz] * (1 + 1e-12))
     # power-of-two scale never lets a code exceed the format: all |codes| <= 448
     assert np.all(np.abs(TABLE[codes]) <= 448)
+
+
+def test_bf16_rows_at_exact_midpoints_match_library_cast(payload):
+    """bf16-valued rows put many x * 448 / amax exactly on an e4m3 rounding midpoint
+    (both are numbers with few significant bits).  There the code depends on
+    both fp32 roundings of the encoding, s = fp32(amax / 448) and fp32(x / s)
+    (the scale rule of MORI GEMM + All-Reduce Benchmark, 'The fp8 wire'), so
+    the oracle's quantisers are held to PyTorch's fp32 division and float8
+    cast on such rows, which hold over 1% exact midpoints."""
+    xb = torch.from_numpy(payload[:256]).to(torch.bfloat16).float()
+    x = xb.numpy()
+    g = xb.view(256, -1, 128)
+    s_ref = g.abs().amax(dim=2) / torch.tensor(448.0, dtype=torch.float32)
+    q_ref = (g / s_ref[:, :, None]).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).reshape(256, -1)
+    q, s = oracle.quant_block(x, 1, 128)
+    assert np.array_equal(s, s_ref.numpy()) and np.array_equal(q, q_ref.numpy())
+    # how many values sit exactly on a midpoint next to their code (products of few-bit numbers are exact)
+    xa = np.abs(x.reshape(256, -1, 128).astype(np.float64))
+    am = xa.max(axis=2, keepdims=True)
+    c = q.reshape(xa.shape).astype(np.int64) & 0x7F
+    v = np.abs(TABLE[c])
+    lo, hi = np.abs(TABLE[np.clip(c - 1, 0, 126)]), np.abs(TABLE[np.clip(c + 1, 0, 126)])
+    mid = (xa > 0) & ((xa * 448.0 == (v + lo) / 2 * am) | (xa * 448.0 == (v + hi) / 2 * am))
+    assert mid.mean() > 0.01
+    qr, sr = oracle.rowquant(x)
+    sr_ref = xb.abs().amax(dim=1) / torch.tensor(448.0, dtype=torch.float32)
+    qr_ref = (xb / sr_ref[:, None]).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(sr, sr_ref.numpy()) and np.array_equal(qr, qr_ref)
+
+
+def test_two_roundings_at_a_midpoint_closed_form():
+    """Worked by hand in exact arithmetic.  amax = 3.5 gives s = 2^-7 exactly:
+    3.375 / s = 432 ties between 416 (0x7D) and 448 (0x7E) and takes the even
+    code 0x7E; 3.125 / s = 400 ties between 384 (0x7C) and 416 and takes 0x7C.
+    amax = 2.03125 = 2 + 2^-5 gives s = fp32(amax / 448) just below amax / 448,
+    so x = 0.0029754638671875 (a bf16 value, x * 448 / amax = 0.65625 exactly)
+    has x / s a little above the midpoint 0.65625 of 0.625 (0x32) and 0.6875
+    (0x33), by less than half an fp32 step: fp32(x / s) is the midpoint itself
+    and ties to the even code 0x32.  Rounding the exact quotient straight to
+    e4m3 would give 0x33."""
+    x = np.array([[3.5, 3.375, 3.125, -3.375], [2.03125, 0.0029754638671875, -0.0029754638671875, 1.0]],
+                 dtype=np.float32)
+    q, s = oracle.rowquant(x)
+    assert s[0] == np.float32(2.0 ** -7)
+    assert list(q[0]) == [0x7E, 0x7E, 0x7C, 0xFE]
+    assert np.float32(2.03125) / np.float32(448.0) == s[1] and np.float64(s[1]) < 2.03125 / 448.0
+    assert q[1, 1] == 0x32 and q[1, 2] == 0xB2
+    qb, sb = oracle.quant_block(x, 1, 4)
+    assert np.array_equal(qb, q) and np.array_equal(sb[:, 0], s)
