@@ -213,6 +213,48 @@ def test_quant_blockscale_bf16_wo_b_activation(g, ctx):
     assert np.array_equal(q.cpu().numpy(), q_ref)
 
 
+def _amax_sweep_bits(C=2048):
+    """bf16 bit patterns [R, C]: every 128-wide group starts with its amax, taken
+    over all 128 bf16 significands at exponents from -122 (amax / 448 below the
+    smallest scale the encoder's guarded products take, down to subnormal
+    scales) to 127, followed by
+    seeded bf16 patterns at or below it with alternating signs (subnormal bf16
+    included).  Exact e4m3 midpoints of x / s occur for every amax significand."""
+    exps = np.array(list(range(-122, -100)) + list(range(-20, 20, 3)) + list(range(100, 128)))
+    amax = (((exps[:, None] + 127) << 7) | (np.arange(128)[None, :])).reshape(-1).astype(np.uint32)
+    rng = np.random.default_rng(11)
+    body = np.floor(rng.random((amax.size, 127)) * (amax[:, None] + 1)).astype(np.uint32)
+    body |= (np.arange(127, dtype=np.uint32) % 2)[None, :] << 15
+    bits = np.concatenate([amax[:, None], body], axis=1).astype(np.uint16)
+    return bits.reshape(-1, C)
+
+
+def test_quantisers_over_an_amax_sweep(g, ctx):
+    """The 1x128, row and mx quantisers on bf16 rows whose groups' amax runs over
+    every significand and exponent: codes and scales bit for bit against the
+    oracle (the guarded encoder's fast path, its division fallback at exact
+    midpoints and its exact path below the smallest scale)."""
+    bits = _amax_sweep_bits()
+    R, C = bits.shape
+    xd = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    xw = xd.float().cpu().numpy()
+    q = torch.empty((R, C), dtype=torch.uint8, device="cuda")
+    s = torch.empty((R, C // 128), dtype=torch.float32, device="cuda")
+    g.quant_blockscale_e4m3(ctx, xd, 1, q, s)
+    qm = torch.empty((R, C), dtype=torch.uint8, device="cuda")
+    em = torch.empty((R, C // 32), dtype=torch.uint8, device="cuda")
+    g.quant_mx_e4m3(ctx, xd, qm, em)
+    qr, sr, _ = codec_gpu(g, ctx, xd)
+    assert_status_ok(g, ctx)
+    q_ref, s_ref = oracle.quant_block(xw, 1, 128)
+    assert np.array_equal(s.cpu().numpy(), s_ref)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    qm_ref, em_ref = oracle.quant_mx(xw)
+    assert np.array_equal(em.cpu().numpy(), em_ref) and np.array_equal(qm.cpu().numpy(), qm_ref)
+    qr_ref, sr_ref = oracle.rowquant(xw)
+    assert np.array_equal(sr, sr_ref) and np.array_equal(qr, qr_ref)
+
+
 # ---------------------------------------------------------------- band reduce
 
 @pytest.mark.parametrize("P,M,N,bands", [(2, 256, 512, 2), (8, 512, 256, 8), (1, 128, 128, 1),
