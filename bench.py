@@ -608,6 +608,16 @@ def run_ours(args, rank, world, local_rank):
                                        "1x128 groups; 40 back-to-back calls rotating over four input sets "
                                        "(256 MiB of input, larger than L2)"}
 
+    def serial_leg(step_fn):
+        """A fused layer with GEMMAR_SERIAL_REDUCE: (GEMM ms, reduce ms, layer ms) per call."""
+        for _ in range(2):
+            step_fn()
+        g.gemmar_set_phase_timing(ctx, True)
+        ms = time_steps(step_fn, max(5, args.steps // 4), stream)
+        g.gemmar_set_phase_timing(ctx, False)
+        ph, calls = g.gemmar_phase_times(ctx)
+        return ph["gemm"] / max(calls, 1), ph["reduce"] / max(calls, 1), ms
+
     # ---- the mxfp8 variant (P = 4 slices, ue8m0 1x32 scales)
     del A, sa
     torch.cuda.empty_cache()
@@ -631,11 +641,22 @@ def run_ours(args, rank, world, local_rank):
     g.gemmar_set_phase_timing(ctx, False)
     mph, mcalls = g.gemmar_phase_times(ctx)
     mx_gemm_ms = mph["gemm"] / max(mcalls, 1)
+    mx_ov, mx_all = g.gemmar_overlap_stats(ctx)
+    mx_se_gemm_ms, mx_se_red_ms, ms_mx_se = serial_leg(
+        lambda: g.fused_gemm_reduce(ctx, Amx, eam, Bmx, ebm, out, scale_kind=g.GEMMAR_SCALE_MX32, bands=Pm,
+                                    flags=g.GEMMAR_SERIAL_REDUCE))
     extra["mxfp8"] = {"workload": "P=4 slices of M=16384 N=7168 K=2048, ue8m0 1x32 scales",
                       "us_per_layer": ms_mx * 1e3,
                       "gemm_us": mx_gemm_ms * 1e3,
                       "gemm_tflops": flops(Pm, M, N, K) / (mx_gemm_ms * 1e-3) / 1e12,
                       "gemm_frac_of_fp8_peak": flops(Pm, M, N, K) / (mx_gemm_ms * 1e-3) / 1e12 / fp8_peak,
+                      "reduce_share_in_gemm": mx_ov / max(mx_all, 1),
+                      "serial_us_per_layer": ms_mx_se * 1e3,
+                      "serial_gemm_us": mx_se_gemm_ms * 1e3,
+                      "serial_reduce_us": mx_se_red_ms * 1e3,
+                      "serial_gemm_frac_of_fp8_peak": flops(Pm, M, N, K) / (mx_se_gemm_ms * 1e-3) / 1e12 / fp8_peak,
+                      "gemm_note": "gemm_us is the band-path launch, which also sums reduce_share_in_gemm of the "
+                                   "band reduce; serial_gemm_us is the GEMM with the whole reduce after it",
                       "slice_loop_us_per_layer": ms_mx_sl * 1e3,
                       "slice_loop_tflops": flops(Pm, M, N, K) / (ms_mx_sl * 1e-3) / 1e12,
                       "onchip_us_per_layer": ms_mx_oc * 1e3,
@@ -655,6 +676,10 @@ def run_ours(args, rank, world, local_rank):
     g.gemmar_set_phase_timing(ctx, False)
     pph, pcalls = g.gemmar_phase_times(ctx)
     pt_gemm_ms = pph["gemm"] / max(pcalls, 1)
+    pt_ov, pt_all = g.gemmar_overlap_stats(ctx)
+    pt_se_gemm_ms, pt_se_red_ms, ms_pt_se = serial_leg(
+        lambda: g.fused_gemm_reduce(ctx, Apt, spa, Bpt, spb, out, scale_kind=g.GEMMAR_SCALE_PTPC, bands=P,
+                                    flags=g.GEMMAR_SERIAL_REDUCE))
     step_pt_oc = lambda: g.fused_gemm_reduce(ctx, Apt, spa, Bpt, spb, out, scale_kind=g.GEMMAR_SCALE_PTPC,
                                              bands=P, flags=g.GEMMAR_FUSE_ONCHIP)
     for _ in range(2):
@@ -665,6 +690,11 @@ def run_ours(args, rank, world, local_rank):
                      "gemm_us": pt_gemm_ms * 1e3,
                      "gemm_tflops": fl / (pt_gemm_ms * 1e-3) / 1e12,
                      "gemm_frac_of_fp8_peak": fl / (pt_gemm_ms * 1e-3) / 1e12 / fp8_peak,
+                     "reduce_share_in_gemm": pt_ov / max(pt_all, 1),
+                     "serial_us_per_layer": ms_pt_se * 1e3,
+                     "serial_gemm_us": pt_se_gemm_ms * 1e3,
+                     "serial_reduce_us": pt_se_red_ms * 1e3,
+                     "serial_gemm_frac_of_fp8_peak": fl / (pt_se_gemm_ms * 1e-3) / 1e12 / fp8_peak,
                      "onchip_us_per_layer": ms_pt_oc * 1e3,
                      "onchip_tflops": fl / (ms_pt_oc * 1e-3) / 1e12,
                      "note": "no per-K-block promotion: the whole K accumulates in TMEM, scaled once per "
