@@ -270,11 +270,6 @@ struct Enc {
             return enc4(a, b, c, d, s);
         return enc2_guarded(a, b, s, yl, yh) | (enc2_guarded(c, d, s, yl, yh) << 16);
     }
-    // the four codes of two packed bf16 pairs (low half first)
-    __device__ __forceinline__ uint32_t bf16x4(uint32_t w0, uint32_t w1) const
-    {
-        return (*this)(bf16_lo(w0), bf16_hi(w0), bf16_lo(w1), bf16_hi(w1));
-    }
 };
 
 template <bool BF16>
