@@ -28,7 +28,7 @@ from helpers import blockscale_operands, check_bf16_output, check_f32_output, mx
 pytestmark = pytest.mark.gpu
 
 MAX_M, MAX_N, MAX_K, MAX_P = 1024, 1024, 512, 8
-CASES_PER_KIND = 12
+CASES_PER_KIND = 24
 
 
 def draw_shapes(kind, n, seed):
@@ -132,7 +132,7 @@ def draw_gemm_shapes(kind, n, seed):
             for _ in range(n)]
 
 
-GEMM_CASES = [(kind, *shape) for kind in (0, 1, 2) for shape in draw_gemm_shapes(kind, 6, 7200 + kind)]
+GEMM_CASES = [(kind, *shape) for kind in (0, 1, 2) for shape in draw_gemm_shapes(kind, 10, 7200 + kind)]
 
 
 @pytest.mark.parametrize("kind,M,N,K", GEMM_CASES, ids=[f"k{k}-M{M}-N{N}-K{K}" for k, M, N, K in GEMM_CASES])
@@ -158,7 +158,7 @@ def draw_reduce_shapes(n, seed):
     return out
 
 
-REDUCE_CASES = draw_reduce_shapes(8, 7300)
+REDUCE_CASES = draw_reduce_shapes(16, 7300)
 
 
 @pytest.mark.parametrize("P,M,N,bands", REDUCE_CASES, ids=[f"P{P}-M{M}-N{N}-b{b}" for P, M, N, b in REDUCE_CASES])
@@ -180,7 +180,7 @@ def draw_codec_shapes(n, seed):
              bool(rng.rand() < 0.5)) for _ in range(n)]
 
 
-CODEC_CASES = draw_codec_shapes(8, 7400)
+CODEC_CASES = draw_codec_shapes(16, 7400)
 
 
 @pytest.mark.parametrize("M,N,sigma,bf16", CODEC_CASES,
