@@ -236,7 +236,10 @@ int band_reduce(gemmar_ctx *ctx, const float *W, int P, int64_t M, int64_t N, in
  *   s[m] = fp32(amax_n |x[m,n]| / 448),  q[m,n] = e4m3_rn_sat(fp32(x[m,n] / s[m]))
  * (IEEE division; a zero row gives s = 0 and +0 codes).  One fp32 scale per
  * row ("MORI GEMM + All-Reduce Benchmark", "The fp8 wire"; sglang pull
- * request #40757, "The optional fp8 gather").
+ * request #40757, "The optional fp8 gather").  Non-finite inputs: the amax
+ * skips NaN (a row of NaN alone is a zero row; a NaN value codes to NaN); an
+ * infinite value makes s infinite, so finite values code to +-0 and
+ * infinities to NaN.
  *   x: [M,N] of x_dtype (GEMMAR_DTYPE_BF16 or GEMMAR_DTYPE_F32); q: uint8 [M,N];
  *   row_scale: fp32 [M].  N % 16 == 0.  Bit-exact against the definition.
  */
@@ -257,7 +260,8 @@ int rowdequant_e4m3(gemmar_ctx *ctx, const uint8_t *q, const float *row_scale, i
  * of group_rows x 128 (group_rows 1 for activations, 128 for weights) of an
  * [R,C] matrix x of x_dtype (GEMMAR_DTYPE_BF16 or GEMMAR_DTYPE_F32; bf16 is
  * widened to fp32 exactly); s = fp32(amax/448), q = e4m3_rn_sat(fp32(x/s));
- * a zero group gives s = 0 and +0 codes.  The real call site quantises wo_b's
+ * a zero group gives s = 0 and +0 codes; non-finite values as in
+ * rowquant_e4m3, per group.  The real call site quantises wo_b's
  * bf16 input itself (sglang pull request #43480, "Numerics, measured where
  * the path engages"), so bf16 is the input the layer sees.
  * q: uint8 [R,C]; scales: fp32 [ceil(R/group_rows), C/128].
@@ -271,7 +275,9 @@ int quant_blockscale_e4m3(gemmar_ctx *ctx, const void *x, int x_dtype, int64_t R
  * of x_dtype (GEMMAR_DTYPE_BF16 or GEMMAR_DTYPE_F32), byte =
  * ceil(log2(fp32(amax/448))) + 127 from the IEEE bits (exact at powers of two;
  * sglang pull request #43480, review item 7), clamped to [0,254], 0 for a
- * zero group; q = e4m3_rn_sat(fp32(x * 2^(127-byte))).
+ * zero group; q = e4m3_rn_sat(fp32(x * 2^(127-byte))).  The amax skips NaN; an
+ * infinite value gives byte 254, finite values then code to +-0 and
+ * infinities saturate to +-448.
  * q: uint8 [R,C]; e8m0: uint8 [R, C/32].  C % 32 == 0.  Bit-exact.
  */
 int quant_mx_e4m3(gemmar_ctx *ctx, const void *x, int x_dtype, int64_t R, int64_t C, uint8_t *q,
