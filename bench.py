@@ -553,6 +553,16 @@ def run_ours(args, rank, world, local_rank):
                                      "in shared memory in the reducer's order; output bit-equal to the "
                                      "headline band path (tests), no partial traffic"}
 
+    def serial_leg(step_fn):
+        """A fused layer with GEMMAR_SERIAL_REDUCE: (GEMM ms, reduce ms, layer ms) per call."""
+        for _ in range(2):
+            step_fn()
+        g.gemmar_set_phase_timing(ctx, True)
+        ms = time_steps(step_fn, max(5, args.steps // 4), stream)
+        g.gemmar_set_phase_timing(ctx, False)
+        ph, calls = g.gemmar_phase_times(ctx)
+        return ph["gemm"] / max(calls, 1), ph["reduce"] / max(calls, 1), ms
+
     # ---- the same layer at M = 8192
     M2 = 8192
     step_m2 = lambda: g.fused_gemm_reduce(ctx, [a[:M2] for a in A], [s[:M2] for s in sa], B, sb,
@@ -575,9 +585,18 @@ def run_ours(args, rank, world, local_rank):
     g.gemmar_set_phase_timing(ctx, False)
     m4ph, m4calls = g.gemmar_phase_times(ctx)
     m4_gemm_ms = m4ph["gemm"] / max(m4calls, 1)
+    m4_ov, m4_all = g.gemmar_overlap_stats(ctx)
+    m4_se_gemm_ms, m4_se_red_ms, ms_m4_se = serial_leg(
+        lambda: g.fused_gemm_reduce(ctx, [a[:M4] for a in A], [s[:M4] for s in sa], B, sb, out[:M4], bands=P,
+                                    flags=g.GEMMAR_SERIAL_REDUCE))
     extra["m4096"] = {"us_per_layer": ms_m4 * 1e3, "tflops": flops(P, M4, N, K) / (ms_m4 * 1e-3) / 1e12,
                       "gemm_us": m4_gemm_ms * 1e3, "reduce_us": m4ph["reduce"] / max(m4calls, 1) * 1e3,
                       "gemm_frac_of_fp8_peak": flops(P, M4, N, K) / (m4_gemm_ms * 1e-3) / 1e12 / fp8_peak,
+                      "reduce_share_in_gemm": m4_ov / max(m4_all, 1),
+                      "serial_us_per_layer": ms_m4_se * 1e3,
+                      "serial_gemm_us": m4_se_gemm_ms * 1e3,
+                      "serial_reduce_us": m4_se_red_ms * 1e3,
+                      "serial_gemm_frac_of_fp8_peak": flops(P, M4, N, K) / (m4_se_gemm_ms * 1e-3) / 1e12 / fp8_peak,
                       "l2": "per step 176 MiB of operands read and 940 MB of partials written and read: larger than L2",
                       "what": "the wo_b prefill shape: P=8 slices of M=4096 N=7168 K=2048, band path"}
 
@@ -607,16 +626,6 @@ def run_ours(args, rank, world, local_rank):
                                "what": "quant_blockscale_e4m3 on bf16 [16384, 2048] (one slice's activations), "
                                        "1x128 groups; 40 back-to-back calls rotating over four input sets "
                                        "(256 MiB of input, larger than L2)"}
-
-    def serial_leg(step_fn):
-        """A fused layer with GEMMAR_SERIAL_REDUCE: (GEMM ms, reduce ms, layer ms) per call."""
-        for _ in range(2):
-            step_fn()
-        g.gemmar_set_phase_timing(ctx, True)
-        ms = time_steps(step_fn, max(5, args.steps // 4), stream)
-        g.gemmar_set_phase_timing(ctx, False)
-        ph, calls = g.gemmar_phase_times(ctx)
-        return ph["gemm"] / max(calls, 1), ph["reduce"] / max(calls, 1), ms
 
     # ---- the mxfp8 variant (P = 4 slices, ue8m0 1x32 scales)
     del A, sa
